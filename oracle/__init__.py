@@ -1,0 +1,12 @@
+"""CPU fp64 oracle of the FLARE++ mixer forward (test infrastructure only).
+
+Imported by tests, the package smoke check and the benchmark's CPU-baseline
+leg; never by the library path.
+"""
+from .flarepp_oracle import (EPS, decode, encode, encode_partial, forward, forward_head,
+                             logsumexp_rows, lse_merge, n0, routing_queries, sdpa,
+                             softmax_rows, synthesis, w_eff)
+
+__all__ = ["EPS", "decode", "encode", "encode_partial", "forward", "forward_head",
+           "logsumexp_rows", "lse_merge", "n0", "routing_queries", "sdpa", "softmax_rows",
+           "synthesis", "w_eff"]

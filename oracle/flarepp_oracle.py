@@ -1,0 +1,196 @@
+"""CPU fp64 oracle of the FLARE++ mixer forward. TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, the package smoke check and the benchmark's CPU-baseline
+leg may import this module. The library path never calls it; it shares no code
+with the CUDA kernels (both sides are only fed from the seeded input module).
+
+It is the plain definition written out in float64 with numpy, following the
+FLARE++ paper ("FLARE++: Low-rank attention with attention-synthesized
+routing", arXiv 2608.11519 v2):
+
+* SDPA(Q, K, V) = softmax(Q K^T / sqrt(D)) V, softmax over the keys
+  (Section 3.1, eq. 1), evaluated with the max shift of Appendix B.3 eq. 29.
+* synthesis keys K~ = N0(Ks_raw), shared as values (Section 3.2 eq. 5,
+  Appendix A.3 eq. 14, A.6 eq. 19).
+* Q^d = SDPA(Qseed, K~, K~) (eq. 6 / eq. 19).
+* Q = N0(Q^f) + g * Q^d (eq. 7 / eq. 15).
+* Z = SDPA(Q, K, V), L = log-sum-exp of the encode scores (eq. 8, B.2 eq. 25).
+* Y = SDPA(K, Q, Z), softmax over the M routes (eq. 8, Figure 1 caption).
+
+Readings where the paper is silent (each one is also listed in the design
+notes of the repository):
+
+1. N0 is RMSNorm without scale over the head width D with eps = 1e-6 inside the
+   square root; the paper gives no eps.
+2. Qseed arrives with its learned-scale normalisation N_a already applied, and
+   K with its N_a applied (eq. 6 and the routing keys of eq. 8); the oracle uses
+   both as given.
+3. ``gate`` is g = sigmoid(gamma) itself, one value per head.
+4. All three calls use the scale 1/sqrt(D), so the decode scores are the
+   transpose of the encode scores.
+5. No intermediate rounding: the oracle takes the (already dtype-rounded)
+   inputs to float64 and rounds nothing afterwards.
+
+Row blocking (``rows``) only splits independent softmax rows into groups to
+bound memory; every row is computed by the same formula.
+
+Parity status: every function here is pinned by tests against closed forms,
+invariants, library routines and brute force; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+EPS = 1e-6
+
+
+def n0(x: np.ndarray, eps: float = EPS) -> np.ndarray:
+    """Affine-free RMSNorm over the last axis, N0 (Section 3.2, eq. 5).
+
+    Each row is divided by sqrt(mean of squares + eps), so it has unit RMS up to
+    the eps term.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps)
+
+
+def softmax_rows(s: np.ndarray) -> np.ndarray:
+    """Row softmax over the last axis with the max shift (Appendix B.3 eq. 29)."""
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def logsumexp_rows(s: np.ndarray) -> np.ndarray:
+    """log sum_j exp(s_j) over the last axis, via the shift identity (eq. 29)."""
+    m = np.max(s, axis=-1, keepdims=True)
+    return (m + np.log(np.sum(np.exp(s - m), axis=-1, keepdims=True)))[..., 0]
+
+
+def sdpa(q: np.ndarray, k: np.ndarray, v: np.ndarray, with_lse: bool = False,
+         rows: int | None = None):
+    """SDPA(Q, K, V) of eq. 1 for one head: q [Nq, D], k [Nk, D], v [Nk, Dv].
+
+    Scores are q k^T / sqrt(D) with D = q.shape[-1]; the softmax runs over the
+    Nk keys. With ``with_lse`` it also returns the row log-normaliser L of
+    Appendix B.2 eq. 25. ``rows`` caps how many query rows are scored at once.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    nq, d = q.shape
+    scale = 1.0 / math.sqrt(d)
+    step = nq if rows is None else max(1, rows)
+    out = np.empty((nq, v.shape[1]), dtype=np.float64)
+    lse = np.empty(nq, dtype=np.float64)
+    for r0 in range(0, nq, step):
+        r1 = min(nq, r0 + step)
+        s = (q[r0:r1] @ k.T) * scale
+        out[r0:r1] = softmax_rows(s) @ v
+        if with_lse:
+            lse[r0:r1] = logsumexp_rows(s)
+    return (out, lse) if with_lse else out
+
+
+def synthesis(qseed_h: np.ndarray, ks_raw_bh: np.ndarray, rows: int | None = None) -> np.ndarray:
+    """Synthesised corrections Q^d = SDPA(Qseed, N0(Ks_raw), N0(Ks_raw)).
+
+    Section 3.2 eq. 5-6 with shared keys and values (Appendix A.6 eq. 19).
+    qseed_h [M, D], ks_raw_bh [N, D] -> [M, D].
+    """
+    kt = n0(ks_raw_bh)
+    return sdpa(qseed_h, kt, kt, rows=rows)
+
+
+def routing_queries(qf_h: np.ndarray, qd: np.ndarray, g: float) -> np.ndarray:
+    """Q = N0(Q^f) + g Q^d (Section 3.2 eq. 7, Appendix A.4 eq. 15)."""
+    return n0(qf_h) + float(g) * np.asarray(qd, dtype=np.float64)
+
+
+def encode(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: int | None = None):
+    """Z = SDPA(Q, K, V) and its log-normaliser L (eq. 8; Appendix B.2 eq. 23-25).
+
+    q [M, D], k [N, D], v [N, D] -> Z [M, D], L [M]; softmax over the N tokens.
+    """
+    return sdpa(q, k, v, with_lse=True, rows=rows)
+
+
+def decode(k: np.ndarray, q: np.ndarray, z: np.ndarray, rows: int | None = None) -> np.ndarray:
+    """Y = SDPA(K, Q, Z): each token attends over the M routes (eq. 8).
+
+    k [N, D], q [M, D], z [M, D] -> [N, D]; softmax over M (Figure 1 caption).
+    """
+    return sdpa(k, q, z, rows=rows)
+
+
+def forward_head(k, v, ks_raw, qseed_h, qf_h, g, rows: int | None = None) -> dict:
+    """The whole mixer for one (batch, head): returns Qd, Q, Z, L and Y."""
+    qd = synthesis(qseed_h, ks_raw, rows=rows)
+    q = routing_queries(qf_h, qd, g)
+    z, lse = encode(q, k, v, rows=rows)
+    y = decode(k, q, z, rows=rows)
+    return {"Qd": qd, "Q": q, "Z": z, "L": lse, "Y": y}
+
+
+def forward(K, V, Ks_raw, Qseed, Qf, gate, rows: int | None = None) -> dict:
+    """The mixer over all batches and heads.
+
+    K, V, Ks_raw [B,H,N,D]; Qseed, Qf [H,M,D]; gate [H]. Returns float64 arrays
+    Qd, Q, Z [B,H,M,D], L [B,H,M] and Y [B,H,N,D].
+    """
+    B, H, N, D = K.shape
+    M = Qseed.shape[1]
+    res = {"Qd": np.empty((B, H, M, D)), "Q": np.empty((B, H, M, D)),
+           "Z": np.empty((B, H, M, D)), "L": np.empty((B, H, M)), "Y": np.empty((B, H, N, D))}
+    for b in range(B):
+        for h in range(H):
+            r = forward_head(K[b, h], V[b, h], Ks_raw[b, h], Qseed[h], Qf[h], gate[h], rows=rows)
+            for key in res:
+                res[key][b, h] = r[key]
+    return res
+
+
+def encode_partial(q: np.ndarray, k: np.ndarray, v: np.ndarray):
+    """Encoder on one token shard: (Z_r, L_r) of Appendix B.2 eq. 24-26.
+
+    An empty shard returns Z_r = 0 and L_r = -inf (Appendix B.3, last paragraph).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    if k.shape[0] == 0:
+        return np.zeros((q.shape[0], v.shape[1])), np.full(q.shape[0], -np.inf)
+    return sdpa(q, k, v, with_lse=True)
+
+
+def lse_merge(z_parts, l_parts):
+    """Exact merge of shard results by the stable schedule of Appendix B.3.
+
+    L_max = max_r L_r (eq. 30); d_r = exp(L_r - L_max), U_r = d_r Z_r (eq. 31);
+    d = sum d_r, U = sum U_r (eq. 32); Z = U / d, L = L_max + log d (eq. 33).
+    Shards with L_r = -inf contribute d_r = U_r = 0.
+    """
+    l_stack = np.stack([np.asarray(x, dtype=np.float64) for x in l_parts])  # [R, M]
+    z_stack = np.stack([np.asarray(x, dtype=np.float64) for x in z_parts])  # [R, M, D]
+    l_max = np.max(l_stack, axis=0)
+    d_r = np.exp(l_stack - l_max[None, :])
+    u_r = d_r[:, :, None] * z_stack
+    d = np.sum(d_r, axis=0)
+    u = np.sum(u_r, axis=0)
+    return u / d[:, None], l_max + np.log(d)
+
+
+def w_eff(q: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """The N x N operator W_dec W_enc of eq. 4 / eq. 9, materialised.
+
+    W_enc = softmax over N of Q K^T / sqrt(D) ([M, N]); W_dec = softmax over M
+    of K Q^T / sqrt(D) ([N, M]). Only for tiny N: it is what the fused path
+    never builds.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    s = (q @ k.T) / math.sqrt(q.shape[1])
+    w_enc = softmax_rows(s)
+    w_dec = softmax_rows(s.T)
+    return w_dec @ w_enc
