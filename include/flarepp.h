@@ -1,0 +1,132 @@
+/*
+ * flarepp.h — C ABI of the GB300 (sm_103a) FLARE++ mixer forward.
+ *
+ * The operation is the token mixer of "FLARE++: Low-rank attention with
+ * attention-synthesized routing" (arXiv 2608.11519 v2), Section 3.2, for each
+ * batch entry b and head h independently, with s = 1/sqrt(D):
+ *
+ *   Kt  = N0(Ks_raw)                          eq. 5  (RMSNorm, no scale, eps 1e-6)
+ *   Qd  = softmax_N(s Qseed Kt^T) Kt          eq. 6 / eq. 19 (keys shared as values)
+ *   Q   = N0(Qf) + g Qd   (fp32, then cast)   eq. 7 / eq. 15
+ *   Z   = softmax_N(s Q K^T) V,  L = LSE_N    eq. 8, Appendix B.2 eq. 23-25
+ *   out = softmax_M(s K Q^T) Z                eq. 8 (decode softmax over the M routes)
+ *
+ * Conventions for every entry point below:
+ *   - All tensor pointers are DEVICE pointers on the device that `stream`
+ *     belongs to, contiguous and row-major, 16-byte aligned.
+ *   - K, V, Ks_raw, out: [B, H, N, D] of `dtype`.  Qseed, Qf: [H, M, D] of
+ *     `dtype`.  gate: [H] fp32, the post-sigmoid value g in [0, 1).
+ *   - K is the routing key as used (the caller applies its learned-scale
+ *     RMSNorm N_a); Qseed is the seed as used (N_a already applied); Ks_raw is
+ *     taken before N0, and Qf before N0 — the library applies both N0s.
+ *   - N is the exact token count of every batch entry; there is no mask.
+ *   - Supported: D in {16, 32}; 1 <= M <= 512 (bf16: M % 16 == 0); N >= 1;
+ *     B*H*N*D < 2^31 elements per tensor.
+ *   - The caller owns every buffer. The library keeps no pointer after return.
+ *   - Calls are asynchronous on `stream`; a returned FLAREPP_OK means the work
+ *     was enqueued. Argument errors are detected before anything is launched.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef FLAREPP_H_
+#define FLAREPP_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FLAREPP_BF16 = 0, FLAREPP_FP32 = 1 } flarepp_dtype_t;
+
+typedef enum {
+  FLAREPP_OK = 0,
+  FLAREPP_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, out aliasing an input */
+  FLAREPP_ERR_UNSUPPORTED = 2,  /* D, M or dtype outside the supported set */
+  FLAREPP_ERR_ALIGNMENT = 3,    /* a pointer not 16-byte aligned */
+  FLAREPP_ERR_NO_MEMORY = 4,    /* workspace could not be allocated or is too small */
+  FLAREPP_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
+  FLAREPP_ERR_TIMEOUT = 6       /* a device-side bounded wait gave up (see flarepp_sync_status) */
+} flarepp_status_t;
+
+/*
+ * The full mixer forward (all six steps above) for B batch entries and H
+ * heads, writing out[B,H,N,D]. Workspace comes from a per-device,
+ * per-stream cache inside the library (stream-ordered cudaMallocAsync,
+ * guarded by a mutex); it grows on demand and is reused across calls on the
+ * same stream. Use flarepp_forward_ws to pass workspace explicitly instead.
+ */
+flarepp_status_t flarepp_forward(const void* K, const void* V, const void* Ks_raw,
+                                 const void* Qseed, const void* Qf, const float* gate,
+                                 int B, int H, int N, int M, int D, flarepp_dtype_t dtype,
+                                 void* out, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace that flarepp_forward_ws needs for these sizes
+ * (split-N partial results, arrival counters, the routing queries Q and the
+ * latents Z). Returns 0 if the sizes are unsupported.
+ */
+size_t flarepp_workspace_size(int B, int H, int N, int M, int D, flarepp_dtype_t dtype);
+
+/*
+ * As flarepp_forward, with caller-owned device workspace of at least
+ * flarepp_workspace_size(...) bytes, 256-byte aligned. The library allocates
+ * nothing on this path. Two calls that run at the same time on the GPU must
+ * not share one workspace.
+ */
+flarepp_status_t flarepp_forward_ws(const void* K, const void* V, const void* Ks_raw,
+                                    const void* Qseed, const void* Qf, const float* gate,
+                                    int B, int H, int N, int M, int D, flarepp_dtype_t dtype,
+                                    void* out, void* workspace, size_t ws_bytes,
+                                    cudaStream_t stream);
+
+/*
+ * As flarepp_forward, and also copies the intermediate results of the
+ * steps, each as fp32 device arrays (any may be NULL):
+ *   Qd_out [B,H,M,D] the merged synthesis output of eq. 6 (before the gate);
+ *   Q_out  [B,H,M,D] the routing queries of eq. 7 as the kernels use them
+ *                    (rounded to `dtype`);
+ *   Z_out  [B,H,M,D] the encoded latents of eq. 8 as used by the decode
+ *                    (rounded to `dtype`);
+ *   L_out  [B,H,M]   the encode log-normaliser (natural log).
+ */
+flarepp_status_t flarepp_forward_debug(const void* K, const void* V, const void* Ks_raw,
+                                       const void* Qseed, const void* Qf, const float* gate,
+                                       int B, int H, int N, int M, int D, flarepp_dtype_t dtype,
+                                       void* out, float* Qd_out, float* Q_out, float* Z_out,
+                                       float* L_out, cudaStream_t stream);
+
+/*
+ * Waits for `stream`, then reports (and clears) any device-side error that
+ * the library's kernels recorded since the last call on this device:
+ * FLAREPP_ERR_TIMEOUT if a bounded wait gave up, FLAREPP_ERR_CUDA if the
+ * stream reported a CUDA error, FLAREPP_OK otherwise.
+ */
+flarepp_status_t flarepp_sync_status(cudaStream_t stream);
+
+/* A static, human-readable name of a status code. Never NULL. */
+const char* flarepp_status_string(flarepp_status_t status);
+
+/*
+ * Test hook: the number of token splits per (batch, head) that the next calls
+ * use for the two split-N passes; 0 restores the automatic choice. The result
+ * does not depend on the split count beyond floating-point rounding (the
+ * log-sum-exp merge of Appendix B.2-B.3 is exact in exact arithmetic).
+ */
+void flarepp_set_splits(int splits);
+
+/*
+ * Measurement hook: while set (events != NULL, count >= 4), every forward call
+ * records events[0] before its first kernel, events[1] after the synthesis
+ * pass (steps a1-a3), events[2] after the encode pass (a4-a5) and events[3]
+ * after the decode (a6), all on the call's stream, so cudaEventElapsedTime
+ * gives each pass's device time. The array is caller-owned and must outlive
+ * the calls; pass NULL to clear. Not thread-safe: for benchmarks and tests.
+ */
+void flarepp_set_stage_events(cudaEvent_t* events, int count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLAREPP_H_ */

@@ -1,0 +1,346 @@
+// Host side of the FLARE++ mixer forward: argument validation, the workspace
+// plan and cache, the split heuristic and the kernel launches behind the C
+// ABI of include/flarepp.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "flarepp.h"
+#include "common.cuh"
+#include "simt.cuh"
+
+namespace flarepp {
+namespace {
+
+std::atomic<int> g_forced_splits{0};
+cudaEvent_t* g_stage_events = nullptr;
+
+void stage_event(int i, cudaStream_t stream) {
+  if (g_stage_events != nullptr) cudaEventRecord(g_stage_events[i], stream);
+}
+
+struct Problem {
+  const void* K;
+  const void* V;
+  const void* Ks;
+  const void* Qseed;
+  const void* Qf;
+  const float* gate;
+  int B, H, N, M, D;
+  flarepp_dtype_t dtype;
+  void* out;
+  float* dbg_qd;
+  float* dbg_q;
+  float* dbg_z;
+  float* dbg_l;
+};
+
+size_t elem_size(flarepp_dtype_t t) { return t == FLAREPP_BF16 ? 2 : 4; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const char* pa = static_cast<const char*>(a);
+  const char* pb = static_cast<const char*>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+flarepp_status_t check_sizes(int B, int H, int N, int M, int D, flarepp_dtype_t dtype) {
+  if (B <= 0 || H <= 0 || N <= 0 || M <= 0 || D <= 0) return FLAREPP_ERR_INVALID_ARG;
+  if (dtype != FLAREPP_BF16 && dtype != FLAREPP_FP32) return FLAREPP_ERR_UNSUPPORTED;
+  if (D != 16 && D != 32) return FLAREPP_ERR_UNSUPPORTED;
+  if (M > 512) return FLAREPP_ERR_UNSUPPORTED;
+  if (dtype == FLAREPP_BF16 && M % 16 != 0) return FLAREPP_ERR_UNSUPPORTED;
+  const long long tokens = (long long)B * H * N * D;
+  if (tokens >= (1LL << 31)) return FLAREPP_ERR_UNSUPPORTED;
+  if ((long long)B * H > 65535) return FLAREPP_ERR_UNSUPPORTED;
+  return FLAREPP_OK;
+}
+
+flarepp_status_t validate(const Problem& p) {
+  flarepp_status_t st = check_sizes(p.B, p.H, p.N, p.M, p.D, p.dtype);
+  if (st != FLAREPP_OK) return st;
+  const void* req[] = {p.K, p.V, p.Ks, p.Qseed, p.Qf, p.gate, p.out};
+  for (const void* ptr : req)
+    if (ptr == nullptr) return FLAREPP_ERR_INVALID_ARG;
+  const void* all[] = {p.K, p.V, p.Ks, p.Qseed, p.Qf, p.gate, p.out,
+                       p.dbg_qd, p.dbg_q, p.dbg_z, p.dbg_l};
+  for (const void* ptr : all)
+    if (ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return FLAREPP_ERR_ALIGNMENT;
+  const size_t es = elem_size(p.dtype);
+  const size_t tok = (size_t)p.B * p.H * p.N * p.D * es;
+  const size_t lat = (size_t)p.H * p.M * p.D * es;
+  const std::pair<const void*, size_t> inputs[] = {
+      {p.K, tok}, {p.V, tok}, {p.Ks, tok}, {p.Qseed, lat}, {p.Qf, lat}, {p.gate, (size_t)p.H * 4}};
+  for (const auto& in : inputs)
+    if (overlaps(p.out, tok, in.first, in.second)) return FLAREPP_ERR_INVALID_ARG;
+  return FLAREPP_OK;
+}
+
+// Workspace layout. Both split-N passes run one after the other on the
+// stream, so they share the partial-result buffers; each has its own set of
+// arrival counters, which the last CTA of every group resets to zero.
+struct Plan {
+  int BH = 0, tiles = 0, splits = 0, split_len = 0;
+  size_t off_pz = 0, off_pl = 0, off_cnt = 0, off_q = 0, off_z = 0, total = 0;
+};
+
+int device_sm_count() {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cache[dev] = sms;
+  return sms;
+}
+
+// Enough (split, tile, head) CTAs to give every SM about two, with each split
+// a whole number of staged tiles.
+Plan make_plan(int B, int H, int N, int M, int D, flarepp_dtype_t dtype, int sms) {
+  Plan pl;
+  pl.BH = B * H;
+  pl.tiles = (M + simt::kRows - 1) / simt::kRows;
+  const int quantum = simt::kTile;
+  const int max_splits = std::max(1, (N + quantum - 1) / quantum);
+  int splits = g_forced_splits.load();
+  if (splits <= 0) {
+    const long long groups = (long long)pl.BH * pl.tiles;
+    const long long want = std::max<long long>(1, (2LL * std::max(sms, 1) + groups - 1) / groups);
+    splits = (int)std::min<long long>(want, 256);
+  }
+  splits = std::min(splits, max_splits);
+  int split_len = (N + splits - 1) / splits;
+  split_len = (split_len + quantum - 1) / quantum * quantum;
+  pl.split_len = split_len;
+  pl.splits = (N + split_len - 1) / split_len;
+  const size_t rows = (size_t)pl.BH * pl.tiles * pl.splits * simt::kRows;
+  size_t off = 0;
+  pl.off_pz = off; off = align_up(off + rows * D * sizeof(float), 256);
+  pl.off_pl = off; off = align_up(off + rows * sizeof(float), 256);
+  pl.off_cnt = off; off = align_up(off + 2 * (size_t)pl.BH * pl.tiles * sizeof(unsigned), 256);
+  const size_t lat = (size_t)pl.BH * M * D * elem_size(dtype);
+  pl.off_q = off; off = align_up(off + lat, 256);
+  pl.off_z = off; off = align_up(off + lat, 256);
+  pl.total = off;
+  return pl;
+}
+
+template <typename T, int D>
+flarepp_status_t launch_typed(const Problem& p, const Plan& pl, char* ws, cudaStream_t stream) {
+  Partials part;
+  part.z = reinterpret_cast<float*>(ws + pl.off_pz);
+  part.l = reinterpret_cast<float*>(ws + pl.off_pl);
+  unsigned* counters = reinterpret_cast<unsigned*>(ws + pl.off_cnt);
+  T* qbuf = reinterpret_cast<T*>(ws + pl.off_q);
+  T* zbuf = reinterpret_cast<T*>(ws + pl.off_z);
+  if (cudaMemsetAsync(counters, 0, 2 * (size_t)pl.BH * pl.tiles * sizeof(unsigned), stream) != cudaSuccess)
+    return FLAREPP_ERR_CUDA;
+
+  const dim3 grid(pl.splits, pl.tiles, pl.BH);
+  stage_event(0, stream);
+  simt::SplitArgs<T> sa;
+  sa.keys = static_cast<const T*>(p.Ks);
+  sa.values = static_cast<const T*>(p.Ks);
+  sa.queries = static_cast<const T*>(p.Qseed);
+  sa.qf = static_cast<const T*>(p.Qf);
+  sa.gate = p.gate;
+  sa.H = p.H; sa.N = p.N; sa.M = p.M;
+  sa.tiles = pl.tiles; sa.splits = pl.splits; sa.split_len = pl.split_len;
+  sa.part = part;
+  sa.part.counters = counters;
+  sa.out = qbuf;
+  sa.dbg_a = p.dbg_qd;
+  sa.dbg_b = p.dbg_q;
+  simt::split_kernel<T, D, true><<<grid, simt::kRows, 0, stream>>>(sa);
+  if (cudaGetLastError() != cudaSuccess) return FLAREPP_ERR_CUDA;
+  stage_event(1, stream);
+
+  simt::SplitArgs<T> ea = sa;
+  ea.keys = static_cast<const T*>(p.K);
+  ea.values = static_cast<const T*>(p.V);
+  ea.queries = qbuf;
+  ea.qf = nullptr;
+  ea.gate = nullptr;
+  ea.part.counters = counters + (size_t)pl.BH * pl.tiles;
+  ea.out = zbuf;
+  ea.dbg_a = p.dbg_z;
+  ea.dbg_b = p.dbg_l;
+  simt::split_kernel<T, D, false><<<grid, simt::kRows, 0, stream>>>(ea);
+  if (cudaGetLastError() != cudaSuccess) return FLAREPP_ERR_CUDA;
+  stage_event(2, stream);
+
+  simt::DecodeArgs<T> da;
+  da.keys = static_cast<const T*>(p.K);
+  da.q = qbuf;
+  da.z = zbuf;
+  da.out = static_cast<T*>(p.out);
+  da.N = p.N;
+  da.M = p.M;
+  const size_t smem = 2 * (size_t)p.M * D * sizeof(float);
+  if (cudaFuncSetAttribute(simt::decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return FLAREPP_ERR_CUDA;
+  const dim3 dgrid((p.N + simt::kDecodeTokens - 1) / simt::kDecodeTokens, pl.BH);
+  simt::decode_kernel<T, D><<<dgrid, simt::kDecodeTokens, smem, stream>>>(da);
+  if (cudaGetLastError() != cudaSuccess) return FLAREPP_ERR_CUDA;
+  stage_event(3, stream);
+  return FLAREPP_OK;
+}
+
+flarepp_status_t launch(const Problem& p, const Plan& pl, char* ws, cudaStream_t stream) {
+  if (p.dtype == FLAREPP_FP32) {
+    return p.D == 16 ? launch_typed<float, 16>(p, pl, ws, stream)
+                     : launch_typed<float, 32>(p, pl, ws, stream);
+  }
+  return p.D == 16 ? launch_typed<__nv_bfloat16, 16>(p, pl, ws, stream)
+                   : launch_typed<__nv_bfloat16, 32>(p, pl, ws, stream);
+}
+
+// Per-(device, stream) workspace cache, stream-ordered allocation.
+struct CachedBuf {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_cache_mu;
+std::map<std::pair<int, cudaStream_t>, CachedBuf> g_cache;
+
+flarepp_status_t cached_workspace(size_t bytes, cudaStream_t stream, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLAREPP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  CachedBuf& buf = g_cache[{dev, stream}];
+  if (buf.bytes >= bytes) {
+    *out = buf.ptr;
+    return FLAREPP_OK;
+  }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return FLAREPP_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return FLAREPP_ERR_NO_MEMORY;  // grow outside capture
+  if (buf.ptr != nullptr) {
+    if (cudaFreeAsync(buf.ptr, stream) != cudaSuccess) return FLAREPP_ERR_CUDA;
+    buf.ptr = nullptr;
+    buf.bytes = 0;
+  }
+  void* p = nullptr;
+  const size_t want = align_up(bytes, 1 << 20);
+  if (cudaMallocAsync(&p, want, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FLAREPP_ERR_NO_MEMORY;
+  }
+  buf.ptr = p;
+  buf.bytes = want;
+  *out = p;
+  return FLAREPP_OK;
+}
+
+flarepp_status_t run(const Problem& p, void* workspace, size_t ws_bytes, bool use_cache,
+                     cudaStream_t stream) {
+  flarepp_status_t st = validate(p);
+  if (st != FLAREPP_OK) return st;
+  const int sms = device_sm_count();
+  if (sms <= 0) return FLAREPP_ERR_CUDA;
+  const Plan pl = make_plan(p.B, p.H, p.N, p.M, p.D, p.dtype, sms);
+  if (use_cache) {
+    st = cached_workspace(pl.total, stream, &workspace);
+    if (st != FLAREPP_OK) return st;
+  } else {
+    if (workspace == nullptr || ws_bytes < pl.total) return FLAREPP_ERR_NO_MEMORY;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FLAREPP_ERR_ALIGNMENT;
+  }
+  return launch(p, pl, static_cast<char*>(workspace), stream);
+}
+
+Problem make_problem(const void* K, const void* V, const void* Ks, const void* Qseed, const void* Qf,
+                     const float* gate, int B, int H, int N, int M, int D, flarepp_dtype_t dtype,
+                     void* out) {
+  Problem p{};
+  p.K = K; p.V = V; p.Ks = Ks; p.Qseed = Qseed; p.Qf = Qf; p.gate = gate;
+  p.B = B; p.H = H; p.N = N; p.M = M; p.D = D; p.dtype = dtype; p.out = out;
+  return p;
+}
+
+}  // namespace
+}  // namespace flarepp
+
+using flarepp::Problem;
+
+extern "C" {
+
+flarepp_status_t flarepp_forward(const void* K, const void* V, const void* Ks_raw, const void* Qseed,
+                                 const void* Qf, const float* gate, int B, int H, int N, int M, int D,
+                                 flarepp_dtype_t dtype, void* out, cudaStream_t stream) {
+  const Problem p = flarepp::make_problem(K, V, Ks_raw, Qseed, Qf, gate, B, H, N, M, D, dtype, out);
+  return flarepp::run(p, nullptr, 0, true, stream);
+}
+
+size_t flarepp_workspace_size(int B, int H, int N, int M, int D, flarepp_dtype_t dtype) {
+  if (flarepp::check_sizes(B, H, N, M, D, dtype) != FLAREPP_OK) return 0;
+  const int sms = flarepp::device_sm_count();
+  if (sms <= 0) return 0;
+  return flarepp::make_plan(B, H, N, M, D, dtype, sms).total;
+}
+
+flarepp_status_t flarepp_forward_ws(const void* K, const void* V, const void* Ks_raw,
+                                    const void* Qseed, const void* Qf, const float* gate, int B,
+                                    int H, int N, int M, int D, flarepp_dtype_t dtype, void* out,
+                                    void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  const Problem p = flarepp::make_problem(K, V, Ks_raw, Qseed, Qf, gate, B, H, N, M, D, dtype, out);
+  return flarepp::run(p, workspace, ws_bytes, false, stream);
+}
+
+flarepp_status_t flarepp_forward_debug(const void* K, const void* V, const void* Ks_raw,
+                                       const void* Qseed, const void* Qf, const float* gate, int B,
+                                       int H, int N, int M, int D, flarepp_dtype_t dtype, void* out,
+                                       float* Qd_out, float* Q_out, float* Z_out, float* L_out,
+                                       cudaStream_t stream) {
+  Problem p = flarepp::make_problem(K, V, Ks_raw, Qseed, Qf, gate, B, H, N, M, D, dtype, out);
+  p.dbg_qd = Qd_out;
+  p.dbg_q = Q_out;
+  p.dbg_z = Z_out;
+  p.dbg_l = L_out;
+  return flarepp::run(p, nullptr, 0, true, stream);
+}
+
+flarepp_status_t flarepp_sync_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FLAREPP_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, flarepp::g_error_word, sizeof(word)) != cudaSuccess)
+    return FLAREPP_ERR_CUDA;
+  if (word != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(flarepp::g_error_word, &zero, sizeof(zero)) != cudaSuccess)
+      return FLAREPP_ERR_CUDA;
+    return (word & flarepp::kErrTimeout) ? FLAREPP_ERR_TIMEOUT : FLAREPP_ERR_CUDA;
+  }
+  return FLAREPP_OK;
+}
+
+const char* flarepp_status_string(flarepp_status_t status) {
+  switch (status) {
+    case FLAREPP_OK: return "ok";
+    case FLAREPP_ERR_INVALID_ARG: return "invalid argument";
+    case FLAREPP_ERR_UNSUPPORTED: return "unsupported size or dtype";
+    case FLAREPP_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case FLAREPP_ERR_NO_MEMORY: return "workspace unavailable or too small";
+    case FLAREPP_ERR_CUDA: return "CUDA error";
+    case FLAREPP_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+void flarepp_set_splits(int splits) { flarepp::g_forced_splits.store(splits < 0 ? 0 : splits); }
+
+void flarepp_set_stage_events(cudaEvent_t* events, int count) {
+  flarepp::g_stage_events = (events != nullptr && count >= 4) ? events : nullptr;
+}
+
+}  // extern "C"

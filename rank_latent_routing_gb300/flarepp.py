@@ -1,0 +1,196 @@
+"""Python binding of the FLARE++ C-ABI library (argument marshalling only).
+
+Every step of the mixer runs in the library's CUDA kernels; this module only
+checks tensor properties, passes device pointers, sizes and the current CUDA
+stream through ctypes, and turns status codes into exceptions. PyTorch is
+used for device memory and streams. There is no CPU path: if the library is
+not built, importing this module raises.
+
+The names follow include/flarepp.h: ``forward``, ``forward_ws``,
+``forward_debug``, ``workspace_size``, ``sync_status``, ``status_string``,
+``set_splits``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB
+
+BF16, FP32 = 0, 1
+_STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "NO_MEMORY",
+           5: "CUDA", 6: "TIMEOUT"}
+
+
+class FlareppError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: FLAREPP_ERR_{_STATUS.get(code, code)} ({status_string(code)})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB):
+        raise ImportError(
+            f"FLARE++ CUDA library not found at {LIB}; build it first "
+            "(python -m rank_latent_routing_gb300.build, or __graft_entry__.build())")
+    lib = ctypes.CDLL(LIB)
+    vp, i, f32p, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
+    lib.flarepp_forward.argtypes = [vp, vp, vp, vp, vp, f32p, i, i, i, i, i, i, vp, st]
+    lib.flarepp_forward.restype = ctypes.c_int
+    lib.flarepp_forward_ws.argtypes = [vp, vp, vp, vp, vp, f32p, i, i, i, i, i, i, vp, vp,
+                                       ctypes.c_size_t, st]
+    lib.flarepp_forward_ws.restype = ctypes.c_int
+    lib.flarepp_forward_debug.argtypes = [vp, vp, vp, vp, vp, f32p, i, i, i, i, i, i, vp,
+                                          f32p, f32p, f32p, f32p, st]
+    lib.flarepp_forward_debug.restype = ctypes.c_int
+    lib.flarepp_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.flarepp_workspace_size.restype = ctypes.c_size_t
+    lib.flarepp_sync_status.argtypes = [st]
+    lib.flarepp_sync_status.restype = ctypes.c_int
+    lib.flarepp_status_string.argtypes = [ctypes.c_int]
+    lib.flarepp_status_string.restype = ctypes.c_char_p
+    lib.flarepp_set_splits.argtypes = [i]
+    lib.flarepp_set_splits.restype = None
+    lib.flarepp_set_stage_events.argtypes = [vp, i]
+    lib.flarepp_set_stage_events.restype = None
+    return lib
+
+
+_lib = _load()
+
+
+def status_string(code: int) -> str:
+    return _lib.flarepp_status_string(int(code)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"unsupported dtype {t.dtype}; use torch.bfloat16 or torch.float32")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(K, V, Ks_raw, Qseed, Qf, gate):
+    B, H, N, D = K.shape
+    M = Qseed.shape[1]
+    for name, t, shape in (("K", K, (B, H, N, D)), ("V", V, (B, H, N, D)),
+                           ("Ks_raw", Ks_raw, (B, H, N, D)), ("Qseed", Qseed, (H, M, D)),
+                           ("Qf", Qf, (H, M, D)), ("gate", gate, (H,))):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device != K.device:
+            raise ValueError(f"{name} is on {t.device}, K on {K.device}")
+    if gate.dtype != torch.float32:
+        raise TypeError("gate must be float32")
+    code = _dtype_code(K)
+    for name, t in (("V", V), ("Ks_raw", Ks_raw), ("Qseed", Qseed), ("Qf", Qf)):
+        if _dtype_code(t) != code:
+            raise TypeError(f"{name} dtype {t.dtype} differs from K dtype {K.dtype}")
+    return B, H, N, M, D, code
+
+
+def forward(K, V, Ks_raw, Qseed, Qf, gate, out=None, stream=None):
+    """The FLARE++ mixer forward; returns ``out`` [B,H,N,D] (allocated if None)."""
+    B, H, N, M, D, code = _check(K, V, Ks_raw, Qseed, Qf, gate)
+    if out is None:
+        out = torch.empty_like(K)
+    with torch.cuda.device(K.device):
+        rc = _lib.flarepp_forward(_ptr(K), _ptr(V), _ptr(Ks_raw), _ptr(Qseed), _ptr(Qf),
+                                  _ptr(gate), B, H, N, M, D, code, _ptr(out), _stream(stream))
+    if rc:
+        raise FlareppError(rc, "flarepp_forward")
+    return out
+
+
+def workspace_size(B, H, N, M, D, dtype=torch.bfloat16, device=None) -> int:
+    code = BF16 if dtype == torch.bfloat16 else FP32
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(_lib.flarepp_workspace_size(B, H, N, M, D, code))
+
+
+def forward_ws(K, V, Ks_raw, Qseed, Qf, gate, workspace, out=None, stream=None):
+    """As ``forward`` with a caller-owned workspace (uint8 CUDA tensor)."""
+    B, H, N, M, D, code = _check(K, V, Ks_raw, Qseed, Qf, gate)
+    if out is None:
+        out = torch.empty_like(K)
+    with torch.cuda.device(K.device):
+        rc = _lib.flarepp_forward_ws(_ptr(K), _ptr(V), _ptr(Ks_raw), _ptr(Qseed), _ptr(Qf),
+                                     _ptr(gate), B, H, N, M, D, code, _ptr(out), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream(stream))
+    if rc:
+        raise FlareppError(rc, "flarepp_forward_ws")
+    return out
+
+
+def forward_debug(K, V, Ks_raw, Qseed, Qf, gate, stream=None) -> dict:
+    """The forward plus the intermediate results Qd, Q, Z (fp32 [B,H,M,D]) and
+    L (fp32 [B,H,M]); returns a dict with those and ``Y``."""
+    B, H, N, M, D, code = _check(K, V, Ks_raw, Qseed, Qf, gate)
+    out = torch.empty_like(K)
+    f = dict(device=K.device, dtype=torch.float32)
+    res = {"Qd": torch.empty(B, H, M, D, **f), "Q": torch.empty(B, H, M, D, **f),
+           "Z": torch.empty(B, H, M, D, **f), "L": torch.empty(B, H, M, **f)}
+    with torch.cuda.device(K.device):
+        rc = _lib.flarepp_forward_debug(_ptr(K), _ptr(V), _ptr(Ks_raw), _ptr(Qseed), _ptr(Qf),
+                                        _ptr(gate), B, H, N, M, D, code, _ptr(out),
+                                        _ptr(res["Qd"]), _ptr(res["Q"]), _ptr(res["Z"]),
+                                        _ptr(res["L"]), _stream(stream))
+    if rc:
+        raise FlareppError(rc, "flarepp_forward_debug")
+    res["Y"] = out
+    return res
+
+
+def sync_status(stream=None) -> int:
+    """Waits for the stream; returns the library status code (0 = OK)."""
+    return int(_lib.flarepp_sync_status(_stream(stream)))
+
+
+def set_splits(splits: int) -> None:
+    """Test hook: force the token split count (0 = automatic)."""
+    _lib.flarepp_set_splits(int(splits))
+
+
+class StageTimer:
+    """Device time of the three passes of each forward call (synthesis,
+    encode, decode), from CUDA events the library records on the call's
+    stream. Use as a context manager around one call at a time."""
+
+    def __init__(self):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        self._arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in self.events])
+
+    def __enter__(self):
+        _lib.flarepp_set_stage_events(ctypes.cast(self._arr, ctypes.c_void_p), 4)
+        return self
+
+    def __exit__(self, *exc):
+        _lib.flarepp_set_stage_events(None, 0)
+        return False
+
+    def elapsed_ms(self):
+        """[synthesis, encode, decode] milliseconds of the last call (synchronises)."""
+        self.events[3].synchronize()
+        return [self.events[i].elapsed_time(self.events[i + 1]) for i in range(3)]
+
+
+def raw_call(name: str, *args):
+    """Calls a C-ABI function by name with raw ctypes arguments (tests only)."""
+    return getattr(_lib, name)(*args)

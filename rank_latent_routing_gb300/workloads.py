@@ -86,13 +86,16 @@ def uniform(seed: int, stream: int, count: int, sub: int = 0, start: int = 0) ->
     return out
 
 
-def normal(seed: int, stream: int, count: int, sub: int = 0) -> np.ndarray:
-    """Standard normals by Box-Muller: element 2i and 2i+1 share uniforms 2i, 2i+1."""
+def normal(seed: int, stream: int, count: int, sub: int = 0, start: int = 0) -> np.ndarray:
+    """Standard normals ``start .. start+count-1`` of one sub-stream, by
+    Box-Muller: elements 2i and 2i+1 share uniforms 2i and 2i+1 (``start`` even)."""
+    if start % 2:
+        raise ValueError("start must be even")
     out = np.empty(count, dtype=np.float64)
     npairs = (count + 1) // 2
     for p0 in range(0, npairs, _CHUNK):
         p1 = min(npairs, p0 + _CHUNK)
-        u = uniform(seed, stream, 2 * (p1 - p0), sub, start=2 * p0)
+        u = uniform(seed, stream, 2 * (p1 - p0), sub, start=start + 2 * p0)
         u = u.reshape(-1, 2)
         r = np.sqrt(-2.0 * np.log(u[:, 0]))
         t = (2.0 * math.pi) * u[:, 1]
@@ -174,47 +177,36 @@ CONFIGS = {
 }
 
 
-def _tokens_iid(seed, stream, s: Shape):
-    return normal(seed, stream, s.B * s.H * s.N * s.D).reshape(s.B, s.H, s.N, s.D)
+def _tokens_iid(seed, stream, s: Shape, b: int, h: int):
+    n = s.N * s.D
+    return normal(seed, stream, n, start=(b * s.H + h) * n).reshape(s.N, s.D)
 
 
-def _tokens_lowrank(seed, stream, s: Shape, rank=8, amp=0.5):
-    out = np.empty((s.B, s.H, s.N, s.D), dtype=np.float64)
+def _tokens_lowrank(seed, stream, s: Shape, b: int, h: int, rank=8, amp=0.5):
     noise_amp = math.sqrt(1.0 - amp * amp)
-    for b in range(s.B):
-        for h in range(s.H):
-            sub = 1 + b * s.H + h
-            U = normal(seed, stream, s.N * rank, sub=sub).reshape(s.N, rank)
-            W = normal(seed, stream + 100, rank * s.D, sub=sub).reshape(rank, s.D) / math.sqrt(rank)
-            E = normal(seed, stream + 200, s.N * s.D, sub=sub).reshape(s.N, s.D)
-            out[b, h] = amp * (U @ W) + noise_amp * E
-    return out
+    sub = 1 + b * s.H + h
+    U = normal(seed, stream, s.N * rank, sub=sub).reshape(s.N, rank)
+    W = normal(seed, stream + 100, rank * s.D, sub=sub).reshape(rank, s.D) / math.sqrt(rank)
+    E = normal(seed, stream + 200, s.N * s.D, sub=sub).reshape(s.N, s.D)
+    return amp * (U @ W) + noise_amp * E
 
 
-def _tokens_vocab(seed, stream, s: Shape, vocab=256):
-    ids = (uniform_bits(seed, STREAM_AUX, 0, s.B * s.N) % np.uint64(vocab)).astype(np.int64)
-    ids = ids.reshape(s.B, s.N)
-    out = np.empty((s.B, s.H, s.N, s.D), dtype=np.float64)
-    for h in range(s.H):
-        table = normal(seed, stream, vocab * s.D, sub=1 + h).reshape(vocab, s.D)
-        out[:, h] = table[ids]
-    return out
+def _tokens_vocab(seed, stream, s: Shape, b: int, h: int, vocab=256):
+    ids = (uniform_bits(seed, STREAM_AUX, b * s.N, s.N) % np.uint64(vocab)).astype(np.int64)
+    table = normal(seed, stream, vocab * s.D, sub=1 + h).reshape(vocab, s.D)
+    return table[ids]
 
 
-def _tokens_points(seed, stream, s: Shape, noise=0.1):
-    pts = uniform(seed, STREAM_AUX, s.B * s.N * 3).reshape(s.B, s.N, 3)
-    out = np.empty((s.B, s.H, s.N, s.D), dtype=np.float64)
-    for h in range(s.H):
-        omega = normal(seed, stream, s.D * 3, sub=1 + h).reshape(s.D, 3) * (2.0 * math.pi)
-        phi = uniform(seed, stream + 100, s.D, sub=1 + h) * (2.0 * math.pi)
-        for b in range(s.B):
-            arg = pts[b] @ omega.T + phi  # [N, D]
-            val = np.empty_like(arg)
-            val[:, 0::2] = np.sin(arg[:, 0::2])
-            val[:, 1::2] = np.cos(arg[:, 1::2])
-            eps = normal(seed, stream + 200, s.N * s.D, sub=1 + b * s.H + h).reshape(s.N, s.D)
-            out[b, h] = math.sqrt(2.0) * val + noise * eps
-    return out
+def _tokens_points(seed, stream, s: Shape, b: int, h: int, noise=0.1):
+    pts = uniform(seed, STREAM_AUX, s.N * 3, start=b * s.N * 3).reshape(s.N, 3)
+    omega = normal(seed, stream, s.D * 3, sub=1 + h).reshape(s.D, 3) * (2.0 * math.pi)
+    phi = uniform(seed, stream + 100, s.D, sub=1 + h) * (2.0 * math.pi)
+    arg = pts @ omega.T + phi  # [N, D]
+    val = np.empty_like(arg)
+    val[:, 0::2] = np.sin(arg[:, 0::2])
+    val[:, 1::2] = np.cos(arg[:, 1::2])
+    eps = normal(seed, stream + 200, s.N * s.D, sub=1 + b * s.H + h).reshape(s.N, s.D)
+    return math.sqrt(2.0) * val + noise * eps
 
 
 _STRUCTURES = {
@@ -225,21 +217,69 @@ _STRUCTURES = {
 }
 
 
+def _round(a, dtype):
+    if dtype == "bf16":
+        return round_to_bf16(a)
+    if dtype == "fp32":
+        return None, np.ascontiguousarray(a, dtype=np.float32)
+    raise ValueError(dtype)
+
+
 def make(shape: Shape, dtype: str = "bf16", structure: str = "iid", seed: int = 1,
          name: str = "custom", qseed_scale: float = 1.0) -> Workload:
-    """Draw one workload. ``qseed_scale`` multiplies Qseed (stress inputs)."""
+    """Draw one workload. ``qseed_scale`` multiplies Qseed (stress inputs).
+
+    Token tensors are drawn one (batch, head) slice at a time and rounded per
+    slice, so ``make_head`` reproduces any slice without drawing the rest."""
     s = shape
     gen = _STRUCTURES[structure]
-    raw = {
-        "K": gen(seed, STREAM_K, s),
-        "V": gen(seed, STREAM_V, s),
-        "Ks_raw": gen(seed, STREAM_KS, s),
+    vals, bits = {}, {}
+    for k, stream in (("K", STREAM_K), ("V", STREAM_V), ("Ks_raw", STREAM_KS)):
+        v = np.empty((s.B, s.H, s.N, s.D), dtype=np.float32)
+        bt = np.empty((s.B, s.H, s.N, s.D), dtype=np.uint16) if dtype == "bf16" else None
+        for b in range(s.B):
+            for h in range(s.H):
+                hb, hv = _round(gen(seed, stream, s, b, h), dtype)
+                v[b, h] = hv
+                if bt is not None:
+                    bt[b, h] = hb
+        vals[k] = v
+        if bt is not None:
+            bits[k] = bt
+    for k, a in _latents(shape, seed, qseed_scale).items():
+        hb, hv = _round(a, dtype)
+        vals[k] = hv
+        if hb is not None:
+            bits[k] = hb
+    gate = uniform(seed, STREAM_GATE, s.H).astype(np.float32)
+    return Workload(name, s, dtype, vals["K"], vals["V"], vals["Ks_raw"], vals["Qseed"],
+                    vals["Qf"], gate, bits)
+
+
+def _latents(s: Shape, seed: int, qseed_scale: float = 1.0) -> dict:
+    return {
         "Qseed": normal(seed, STREAM_QSEED, s.H * s.M * s.D).reshape(s.H, s.M, s.D)
         * (qseed_scale / math.sqrt(s.D)),
         "Qf": normal(seed, STREAM_QF, s.H * s.M * s.D).reshape(s.H, s.M, s.D) / math.sqrt(s.D),
     }
-    gate = uniform(seed, STREAM_GATE, s.H).astype(np.float32)
-    return from_arrays(name, s, dtype, gate=gate, **raw)
+
+
+def make_head(name: str, b: int, h: int, **overrides) -> dict:
+    """The (b, h) slice of a named workload, drawn alone: K, V, Ks_raw [N, D],
+    Qseed, Qf [M, D] and the gate g (float), the same values as in ``config``."""
+    shape, dtype, structure, seed = CONFIGS[name]
+    dims = {k: overrides.pop(k, getattr(shape, k)) for k in ("B", "H", "N", "M", "D")}
+    s = Shape(**dims)
+    dtype = overrides.pop("dtype", dtype)
+    seed = overrides.pop("seed", seed)
+    gen = _STRUCTURES[structure]
+    out = {}
+    for k, stream in (("K", STREAM_K), ("V", STREAM_V), ("Ks_raw", STREAM_KS)):
+        out[k] = _round(gen(seed, stream, s, b, h), dtype)[1]
+    for k, a in _latents(s, seed).items():
+        out[k] = _round(a, dtype)[1][h]
+    out["gate"] = float(uniform(seed, STREAM_GATE, s.H).astype(np.float32)[h])
+    return out
 
 
 def from_arrays(name: str, shape: Shape, dtype: str, K, V, Ks_raw, Qseed, Qf, gate) -> Workload:

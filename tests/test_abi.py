@@ -1,0 +1,81 @@
+"""The C-ABI library loads and exports every entry point of include/flarepp.h;
+argument validation works without a GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "flarepp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flarepp_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rank_latent_routing_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path), path
+
+
+def test_header_declares_the_boundary():
+    names = _header_functions()
+    for want in ("flarepp_forward", "flarepp_forward_ws", "flarepp_forward_debug",
+                 "flarepp_workspace_size", "flarepp_sync_status", "flarepp_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    _, path = lib
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (flarepp_\w+)", out))
+    missing = [n for n in _header_functions() if n not in exported]
+    assert not missing, missing
+    for n in _header_functions():
+        getattr(lib[0], n)
+
+
+def test_status_strings(lib):
+    l = lib[0]
+    l.flarepp_status_string.restype = ctypes.c_char_p
+    seen = set()
+    for code in range(7):
+        s = l.flarepp_status_string(code).decode()
+        assert s and s not in seen
+        seen.add(s)
+    assert l.flarepp_status_string(99).decode() == "unknown status"
+
+
+def _forward(l, ptrs, B=1, H=2, N=64, M=32, D=16, dtype=0, out=None):
+    f = l.flarepp_forward
+    vp = ctypes.c_void_p
+    f.argtypes = [vp] * 6 + [ctypes.c_int] * 6 + [vp, vp]
+    f.restype = ctypes.c_int
+    return f(*ptrs, B, H, N, M, D, dtype, out, None)
+
+
+def test_argument_validation_without_gpu(lib):
+    l = lib[0]
+    good = [0x10000 * (i + 1) for i in range(6)]
+    out = 0x900000
+    assert _forward(l, [None] + good[1:], out=out) == 1          # null K
+    assert _forward(l, good, out=None) == 1                      # null out
+    assert _forward(l, good, N=0, out=out) == 1                  # N <= 0
+    assert _forward(l, good, D=64, out=out) == 2                 # D unsupported
+    assert _forward(l, good, M=520, out=out) == 2                # M > 512
+    assert _forward(l, good, M=40, out=out) == 2                 # bf16 needs M % 16 == 0
+    assert _forward(l, good, dtype=7, out=out) == 2              # unknown dtype
+    assert _forward(l, [good[0] + 8] + good[1:], out=out) == 3   # misaligned K
+    assert _forward(l, good, out=good[1]) == 1                   # out aliases V
+
+
+def test_workspace_size_rejects_unsupported(lib):
+    l = lib[0]
+    l.flarepp_workspace_size.restype = ctypes.c_size_t
+    assert l.flarepp_workspace_size(1, 1, 64, 32, 64, 0) == 0
+    assert l.flarepp_workspace_size(1, 1, 0, 32, 16, 0) == 0
