@@ -108,6 +108,13 @@ flarepp_status_t flarepp_sync_status(cudaStream_t stream);
 const char* flarepp_status_string(flarepp_status_t status);
 
 /*
+ * Which CUDA call last failed on the calling thread, with CUDA's error name
+ * and text ("no error" if none). The string is owned by the library and valid
+ * until the thread's next library call.
+ */
+const char* flarepp_last_error(void);
+
+/*
  * Test hook: the number of token splits per (batch, head) that the next calls
  * use for the two split-N passes; 0 restores the automatic choice. The result
  * does not depend on the split count beyond floating-point rounding (the

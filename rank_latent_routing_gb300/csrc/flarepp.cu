@@ -3,6 +3,7 @@
 // ABI of include/flarepp.h.
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <algorithm>
 #include <atomic>
 #include <map>
@@ -17,6 +18,15 @@ namespace flarepp {
 namespace {
 
 std::atomic<int> g_forced_splits{0};
+thread_local char g_last_error[256] = "no error";
+
+// Records which CUDA call failed (for flarepp_last_error) and passes the result on.
+bool cuda_ok(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return true;
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", what, cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return false;
+}
 cudaEvent_t* g_stage_events = nullptr;
 
 void stage_event(int i, cudaStream_t stream) {
@@ -142,7 +152,8 @@ flarepp_status_t launch_typed(const Problem& p, const Plan& pl, char* ws, cudaSt
   unsigned* counters = reinterpret_cast<unsigned*>(ws + pl.off_cnt);
   T* qbuf = reinterpret_cast<T*>(ws + pl.off_q);
   T* zbuf = reinterpret_cast<T*>(ws + pl.off_z);
-  if (cudaMemsetAsync(counters, 0, 2 * (size_t)pl.BH * pl.tiles * sizeof(unsigned), stream) != cudaSuccess)
+  if (!cuda_ok(cudaMemsetAsync(counters, 0, 2 * (size_t)pl.BH * pl.tiles * sizeof(unsigned), stream),
+               "cudaMemsetAsync(counters)"))
     return FLAREPP_ERR_CUDA;
 
   const dim3 grid(pl.splits, pl.tiles, pl.BH);
@@ -161,7 +172,7 @@ flarepp_status_t launch_typed(const Problem& p, const Plan& pl, char* ws, cudaSt
   sa.dbg_a = p.dbg_qd;
   sa.dbg_b = p.dbg_q;
   simt::split_kernel<T, D, true><<<grid, simt::kRows, 0, stream>>>(sa);
-  if (cudaGetLastError() != cudaSuccess) return FLAREPP_ERR_CUDA;
+  if (!cuda_ok(cudaGetLastError(), "launch synthesis")) return FLAREPP_ERR_CUDA;
   stage_event(1, stream);
 
   simt::SplitArgs<T> ea = sa;
@@ -175,7 +186,7 @@ flarepp_status_t launch_typed(const Problem& p, const Plan& pl, char* ws, cudaSt
   ea.dbg_a = p.dbg_z;
   ea.dbg_b = p.dbg_l;
   simt::split_kernel<T, D, false><<<grid, simt::kRows, 0, stream>>>(ea);
-  if (cudaGetLastError() != cudaSuccess) return FLAREPP_ERR_CUDA;
+  if (!cuda_ok(cudaGetLastError(), "launch encode")) return FLAREPP_ERR_CUDA;
   stage_event(2, stream);
 
   simt::DecodeArgs<T> da;
@@ -186,12 +197,13 @@ flarepp_status_t launch_typed(const Problem& p, const Plan& pl, char* ws, cudaSt
   da.N = p.N;
   da.M = p.M;
   const size_t smem = 2 * (size_t)p.M * D * sizeof(float);
-  if (cudaFuncSetAttribute(simt::decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  if (!cuda_ok(cudaFuncSetAttribute(simt::decode_kernel<T, D>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+               "cudaFuncSetAttribute(decode)"))
     return FLAREPP_ERR_CUDA;
   const dim3 dgrid((p.N + simt::kDecodeTokens - 1) / simt::kDecodeTokens, pl.BH);
   simt::decode_kernel<T, D><<<dgrid, simt::kDecodeTokens, smem, stream>>>(da);
-  if (cudaGetLastError() != cudaSuccess) return FLAREPP_ERR_CUDA;
+  if (!cuda_ok(cudaGetLastError(), "launch decode")) return FLAREPP_ERR_CUDA;
   stage_event(3, stream);
   return FLAREPP_OK;
 }
@@ -215,7 +227,7 @@ std::map<std::pair<int, cudaStream_t>, CachedBuf> g_cache;
 
 flarepp_status_t cached_workspace(size_t bytes, cudaStream_t stream, void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FLAREPP_ERR_CUDA;
+  if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice")) return FLAREPP_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_cache_mu);
   CachedBuf& buf = g_cache[{dev, stream}];
   if (buf.bytes >= bytes) {
@@ -223,16 +235,16 @@ flarepp_status_t cached_workspace(size_t bytes, cudaStream_t stream, void** out)
     return FLAREPP_OK;
   }
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return FLAREPP_ERR_CUDA;
+  if (!cuda_ok(cudaStreamIsCapturing(stream, &cap), "cudaStreamIsCapturing")) return FLAREPP_ERR_CUDA;
   if (cap != cudaStreamCaptureStatusNone) return FLAREPP_ERR_NO_MEMORY;  // grow outside capture
   if (buf.ptr != nullptr) {
-    if (cudaFreeAsync(buf.ptr, stream) != cudaSuccess) return FLAREPP_ERR_CUDA;
+    if (!cuda_ok(cudaFreeAsync(buf.ptr, stream), "cudaFreeAsync")) return FLAREPP_ERR_CUDA;
     buf.ptr = nullptr;
     buf.bytes = 0;
   }
   void* p = nullptr;
   const size_t want = align_up(bytes, 1 << 20);
-  if (cudaMallocAsync(&p, want, stream) != cudaSuccess) {
+  if (!cuda_ok(cudaMallocAsync(&p, want, stream), "cudaMallocAsync(workspace)")) {
     cudaGetLastError();
     return FLAREPP_ERR_NO_MEMORY;
   }
@@ -247,7 +259,10 @@ flarepp_status_t run(const Problem& p, void* workspace, size_t ws_bytes, bool us
   flarepp_status_t st = validate(p);
   if (st != FLAREPP_OK) return st;
   const int sms = device_sm_count();
-  if (sms <= 0) return FLAREPP_ERR_CUDA;
+  if (sms <= 0) {
+    snprintf(g_last_error, sizeof(g_last_error), "no CUDA device (cudaGetDevice or attribute query failed)");
+    return FLAREPP_ERR_CUDA;
+  }
   const Plan pl = make_plan(p.B, p.H, p.N, p.M, p.D, p.dtype, sms);
   if (use_cache) {
     st = cached_workspace(pl.total, stream, &workspace);
@@ -311,13 +326,14 @@ flarepp_status_t flarepp_forward_debug(const void* K, const void* V, const void*
 }
 
 flarepp_status_t flarepp_sync_status(cudaStream_t stream) {
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return FLAREPP_ERR_CUDA;
+  using flarepp::cuda_ok;
+  if (!cuda_ok(cudaStreamSynchronize(stream), "cudaStreamSynchronize")) return FLAREPP_ERR_CUDA;
   unsigned word = 0;
-  if (cudaMemcpyFromSymbol(&word, flarepp::g_error_word, sizeof(word)) != cudaSuccess)
+  if (!cuda_ok(cudaMemcpyFromSymbol(&word, flarepp::g_error_word, sizeof(word)), "read error word"))
     return FLAREPP_ERR_CUDA;
   if (word != 0) {
     const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(flarepp::g_error_word, &zero, sizeof(zero)) != cudaSuccess)
+    if (!cuda_ok(cudaMemcpyToSymbol(flarepp::g_error_word, &zero, sizeof(zero)), "clear error word"))
       return FLAREPP_ERR_CUDA;
     return (word & flarepp::kErrTimeout) ? FLAREPP_ERR_TIMEOUT : FLAREPP_ERR_CUDA;
   }
@@ -336,6 +352,8 @@ const char* flarepp_status_string(flarepp_status_t status) {
   }
   return "unknown status";
 }
+
+const char* flarepp_last_error(void) { return flarepp::g_last_error; }
 
 void flarepp_set_splits(int splits) { flarepp::g_forced_splits.store(splits < 0 ? 0 : splits); }
 

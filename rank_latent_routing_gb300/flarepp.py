@@ -27,7 +27,8 @@ _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "NO_M
 class FlareppError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: FLAREPP_ERR_{_STATUS.get(code, code)} ({status_string(code)})")
+        detail = _lib.flarepp_last_error().decode() if code == 5 else status_string(code)
+        super().__init__(f"{where}: FLAREPP_ERR_{_STATUS.get(code, code)} ({detail})")
 
 
 def _load() -> ctypes.CDLL:
@@ -51,6 +52,8 @@ def _load() -> ctypes.CDLL:
     lib.flarepp_sync_status.restype = ctypes.c_int
     lib.flarepp_status_string.argtypes = [ctypes.c_int]
     lib.flarepp_status_string.restype = ctypes.c_char_p
+    lib.flarepp_last_error.argtypes = []
+    lib.flarepp_last_error.restype = ctypes.c_char_p
     lib.flarepp_set_splits.argtypes = [i]
     lib.flarepp_set_splits.restype = None
     lib.flarepp_set_stage_events.argtypes = [vp, i]
