@@ -19,6 +19,7 @@ namespace {
 
 std::atomic<int> g_forced_splits{0};
 thread_local char g_last_error[256] = "no error";
+cudaEvent_t* g_stage_events = nullptr;
 
 // Records which CUDA call failed (for flarepp_last_error) and passes the result on.
 bool cuda_ok(cudaError_t e, const char* what) {
@@ -27,10 +28,10 @@ bool cuda_ok(cudaError_t e, const char* what) {
            cudaGetErrorString(e));
   return false;
 }
-cudaEvent_t* g_stage_events = nullptr;
 
-void stage_event(int i, cudaStream_t stream) {
-  if (g_stage_events != nullptr) cudaEventRecord(g_stage_events[i], stream);
+bool stage_event(int i, cudaStream_t stream) {
+  if (g_stage_events == nullptr) return true;
+  return cuda_ok(cudaEventRecord(g_stage_events[i], stream), "cudaEventRecord(stage event)");
 }
 
 struct Problem {
@@ -157,7 +158,7 @@ flarepp_status_t launch_typed(const Problem& p, const Plan& pl, char* ws, cudaSt
     return FLAREPP_ERR_CUDA;
 
   const dim3 grid(pl.splits, pl.tiles, pl.BH);
-  stage_event(0, stream);
+  if (!stage_event(0, stream)) return FLAREPP_ERR_CUDA;
   simt::SplitArgs<T> sa;
   sa.keys = static_cast<const T*>(p.Ks);
   sa.values = static_cast<const T*>(p.Ks);
@@ -173,7 +174,7 @@ flarepp_status_t launch_typed(const Problem& p, const Plan& pl, char* ws, cudaSt
   sa.dbg_b = p.dbg_q;
   simt::split_kernel<T, D, true><<<grid, simt::kRows, 0, stream>>>(sa);
   if (!cuda_ok(cudaGetLastError(), "launch synthesis")) return FLAREPP_ERR_CUDA;
-  stage_event(1, stream);
+  if (!stage_event(1, stream)) return FLAREPP_ERR_CUDA;
 
   simt::SplitArgs<T> ea = sa;
   ea.keys = static_cast<const T*>(p.K);
@@ -187,7 +188,7 @@ flarepp_status_t launch_typed(const Problem& p, const Plan& pl, char* ws, cudaSt
   ea.dbg_b = p.dbg_l;
   simt::split_kernel<T, D, false><<<grid, simt::kRows, 0, stream>>>(ea);
   if (!cuda_ok(cudaGetLastError(), "launch encode")) return FLAREPP_ERR_CUDA;
-  stage_event(2, stream);
+  if (!stage_event(2, stream)) return FLAREPP_ERR_CUDA;
 
   simt::DecodeArgs<T> da;
   da.keys = static_cast<const T*>(p.K);
@@ -204,7 +205,7 @@ flarepp_status_t launch_typed(const Problem& p, const Plan& pl, char* ws, cudaSt
   const dim3 dgrid((p.N + simt::kDecodeTokens - 1) / simt::kDecodeTokens, pl.BH);
   simt::decode_kernel<T, D><<<dgrid, simt::kDecodeTokens, smem, stream>>>(da);
   if (!cuda_ok(cudaGetLastError(), "launch decode")) return FLAREPP_ERR_CUDA;
-  stage_event(3, stream);
+  if (!stage_event(3, stream)) return FLAREPP_ERR_CUDA;
   return FLAREPP_OK;
 }
 

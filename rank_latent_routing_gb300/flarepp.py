@@ -178,7 +178,12 @@ class StageTimer:
 
     def __init__(self):
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        self._arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in self.events])
+        for e in self.events:  # torch creates the CUDA event on first record
+            e.record()
+        handles = [e.cuda_event for e in self.events]
+        if not all(handles):
+            raise RuntimeError("CUDA events were not created")
+        self._arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(h) for h in handles])
 
     def __enter__(self):
         _lib.flarepp_set_stage_events(ctypes.cast(self._arr, ctypes.c_void_p), 4)
