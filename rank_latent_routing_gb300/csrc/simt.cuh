@@ -66,9 +66,12 @@ __global__ void __launch_bounds__(kRows) split_kernel(const SplitArgs<T> a) {
   for (int n0 = n_begin; n0 < n_end; n0 += kTile) {
     const int cnt = min(kTile, n_end - n0);
     __syncthreads();
-    for (int e = tid; e < cnt * D; e += kRows) {
-      ks[e / D][e % D] = to_f32(a.keys[base + (size_t)n0 * D + e]);
-      if constexpr (!kSynth) vs[e / D][e % D] = to_f32(a.values[base + (size_t)n0 * D + e]);
+    // rows past the split's end are zero-filled: their weights are 0, and
+    // 0 * (stale shared memory) could be NaN
+    for (int e = tid; e < kTile * D; e += kRows) {
+      const bool in = e < cnt * D;
+      ks[e / D][e % D] = in ? to_f32(a.keys[base + (size_t)n0 * D + e]) : 0.f;
+      if constexpr (!kSynth) vs[e / D][e % D] = in ? to_f32(a.values[base + (size_t)n0 * D + e]) : 0.f;
     }
     if (kSynth) {
       // N0 of the synthesis keys (eq. 5): one thread per staged token row
