@@ -97,6 +97,29 @@ flarepp_status_t flarepp_forward_debug(const void* K, const void* V, const void*
                                        float* L_out, cudaStream_t stream);
 
 /*
+ * As flarepp_forward_ws, for callers that cannot allocate device memory: the
+ * scratch lives in one fixed array inside the library (32 MiB per device,
+ * reserved when the library's device code is loaded and kept until the process
+ * exits), so the call itself allocates nothing. The FLARE++ paper has no
+ * counterpart; this exists for host programs whose allocator owns all device
+ * memory, or that may not allocate after start-up, or that must not block on
+ * an allocation inside a timed loop.
+ *   - Returns FLAREPP_ERR_NO_MEMORY when these sizes need more scratch than
+ *     the 32 MiB maximum (flarepp_workspace_size(...) > 32 MiB).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the one array, and it keeps the previous
+ *     call's contents (the library clears what must start at zero). Calls that
+ *     overlap on the GPU — on different streams, or from different host threads
+ *     without ordering between them — race on it and give wrong results;
+ *     serialise them.
+ */
+flarepp_status_t flarepp_forward_static(const void* K, const void* V, const void* Ks_raw,
+                                        const void* Qseed, const void* Qf, const float* gate,
+                                        int B, int H, int N, int M, int D, flarepp_dtype_t dtype,
+                                        void* out, cudaStream_t stream);
+
+/*
  * Waits for `stream`, then reports (and clears) any device-side error that
  * the library's kernels recorded since the last call on this device:
  * FLAREPP_ERR_TIMEOUT if a bounded wait gave up, FLAREPP_ERR_CUDA if the

@@ -46,6 +46,8 @@ def _load() -> ctypes.CDLL:
     lib.flarepp_forward_debug.argtypes = [vp, vp, vp, vp, vp, f32p, i, i, i, i, i, i, vp,
                                           f32p, f32p, f32p, f32p, st]
     lib.flarepp_forward_debug.restype = ctypes.c_int
+    lib.flarepp_forward_static.argtypes = [vp, vp, vp, vp, vp, f32p, i, i, i, i, i, i, vp, st]
+    lib.flarepp_forward_static.restype = ctypes.c_int
     lib.flarepp_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.flarepp_workspace_size.restype = ctypes.c_size_t
     lib.flarepp_sync_status.argtypes = [st]
@@ -139,6 +141,20 @@ def forward_ws(K, V, Ks_raw, Qseed, Qf, gate, workspace, out=None, stream=None):
                                      _stream(stream))
     if rc:
         raise FlareppError(rc, "flarepp_forward_ws")
+    return out
+
+
+def forward_static(K, V, Ks_raw, Qseed, Qf, gate, out, stream=None):
+    """As ``forward``, for callers that cannot allocate device memory: scratch
+    comes from a fixed 32 MiB array inside the library and ``out`` must be
+    given. Calls that overlap on the GPU share that array and race."""
+    B, H, N, M, D, code = _check(K, V, Ks_raw, Qseed, Qf, gate)
+    with torch.cuda.device(K.device):
+        rc = _lib.flarepp_forward_static(_ptr(K), _ptr(V), _ptr(Ks_raw), _ptr(Qseed), _ptr(Qf),
+                                         _ptr(gate), B, H, N, M, D, code, _ptr(out),
+                                         _stream(stream))
+    if rc:
+        raise FlareppError(rc, "flarepp_forward_static")
     return out
 
 
