@@ -12,6 +12,7 @@
 
 #include "flarepp.h"
 #include "common.cuh"
+#include "launch.h"
 #include "simt.cuh"
 
 namespace flarepp {
@@ -97,6 +98,7 @@ flarepp_status_t validate(const Problem& p) {
 // arrival counters, which the last CTA of every group resets to zero.
 struct Plan {
   int BH = 0, tiles = 0, splits = 0, split_len = 0;
+  TcPlan tc{};  // bf16 tensor-core path
   size_t off_pz = 0, off_pl = 0, off_cnt = 0, off_q = 0, off_z = 0, total = 0;
 };
 
@@ -114,26 +116,35 @@ int device_sm_count() {
   return sms;
 }
 
-// Enough (split, tile, head) CTAs to give every SM about two, with each split
-// a whole number of staged tiles.
+// fp32 path: enough (split, tile, head) CTAs to give every SM about two, each
+// split a whole number of staged tiles. bf16 path: tc_plan (tc.cu).
 Plan make_plan(int B, int H, int N, int M, int D, flarepp_dtype_t dtype, int sms) {
   Plan pl;
   pl.BH = B * H;
-  pl.tiles = (M + simt::kRows - 1) / simt::kRows;
-  const int quantum = simt::kTile;
-  const int max_splits = std::max(1, (N + quantum - 1) / quantum);
-  int splits = g_forced_splits.load();
-  if (splits <= 0) {
-    const long long groups = (long long)pl.BH * pl.tiles;
-    const long long want = std::max<long long>(1, (2LL * std::max(sms, 1) + groups - 1) / groups);
-    splits = (int)std::min<long long>(want, 256);
+  size_t rows = 0;
+  if (dtype == FLAREPP_BF16) {
+    pl.tc = tc_plan(B, H, N, M, D, sms, g_forced_splits.load());
+    pl.tiles = pl.tc.tiles;
+    pl.splits = pl.tc.splits;
+    pl.split_len = pl.tc.split_len;
+    rows = (size_t)pl.BH * pl.tiles * pl.splits * pl.tc.streams * 128;
+  } else {
+    pl.tiles = (M + simt::kRows - 1) / simt::kRows;
+    const int quantum = simt::kTile;
+    const int max_splits = std::max(1, (N + quantum - 1) / quantum);
+    int splits = g_forced_splits.load();
+    if (splits <= 0) {
+      const long long groups = (long long)pl.BH * pl.tiles;
+      const long long want = std::max<long long>(1, (2LL * std::max(sms, 1) + groups - 1) / groups);
+      splits = (int)std::min<long long>(want, 256);
+    }
+    splits = std::min(splits, max_splits);
+    int split_len = (N + splits - 1) / splits;
+    split_len = (split_len + quantum - 1) / quantum * quantum;
+    pl.split_len = split_len;
+    pl.splits = (N + split_len - 1) / split_len;
+    rows = (size_t)pl.BH * pl.tiles * pl.splits * simt::kRows;
   }
-  splits = std::min(splits, max_splits);
-  int split_len = (N + splits - 1) / splits;
-  split_len = (split_len + quantum - 1) / quantum * quantum;
-  pl.split_len = split_len;
-  pl.splits = (N + split_len - 1) / split_len;
-  const size_t rows = (size_t)pl.BH * pl.tiles * pl.splits * simt::kRows;
   size_t off = 0;
   pl.off_pz = off; off = align_up(off + rows * D * sizeof(float), 256);
   pl.off_pl = off; off = align_up(off + rows * sizeof(float), 256);
@@ -143,6 +154,28 @@ Plan make_plan(int B, int H, int N, int M, int D, flarepp_dtype_t dtype, int sms
   pl.off_z = off; off = align_up(off + lat, 256);
   pl.total = off;
   return pl;
+}
+
+// bf16: the tensor-core kernels of tc.cu.
+flarepp_status_t launch_tc(const Problem& p, const Plan& pl, char* ws, cudaStream_t stream) {
+  unsigned* counters = reinterpret_cast<unsigned*>(ws + pl.off_cnt);
+  if (!cuda_ok(cudaMemsetAsync(counters, 0, 2 * (size_t)pl.BH * pl.tiles * sizeof(unsigned), stream),
+               "cudaMemsetAsync(counters)"))
+    return FLAREPP_ERR_CUDA;
+  DeviceProblem dp{};
+  dp.K = p.K; dp.V = p.V; dp.Ks = p.Ks; dp.Qseed = p.Qseed; dp.Qf = p.Qf; dp.gate = p.gate;
+  dp.out = p.out;
+  dp.B = p.B; dp.H = p.H; dp.N = p.N; dp.M = p.M; dp.D = p.D;
+  dp.dbg_qd = p.dbg_qd; dp.dbg_q = p.dbg_q; dp.dbg_z = p.dbg_z; dp.dbg_l = p.dbg_l;
+  TcWorkspace w{};
+  w.part_z = reinterpret_cast<float*>(ws + pl.off_pz);
+  w.part_l = reinterpret_cast<float*>(ws + pl.off_pl);
+  w.counters = counters;
+  w.q = ws + pl.off_q;
+  w.z = ws + pl.off_z;
+  const char* failed = "";
+  const cudaError_t e = tc_forward(dp, pl.tc, w, g_stage_events, stream, &failed);
+  return cuda_ok(e, failed) ? FLAREPP_OK : FLAREPP_ERR_CUDA;
 }
 
 template <typename T, int D>
@@ -214,8 +247,7 @@ flarepp_status_t launch(const Problem& p, const Plan& pl, char* ws, cudaStream_t
     return p.D == 16 ? launch_typed<float, 16>(p, pl, ws, stream)
                      : launch_typed<float, 32>(p, pl, ws, stream);
   }
-  return p.D == 16 ? launch_typed<__nv_bfloat16, 16>(p, pl, ws, stream)
-                   : launch_typed<__nv_bfloat16, 32>(p, pl, ws, stream);
+  return launch_tc(p, pl, ws, stream);
 }
 
 // Per-(device, stream) workspace cache, stream-ordered allocation.
@@ -336,6 +368,12 @@ flarepp_status_t flarepp_sync_status(cudaStream_t stream) {
     const unsigned zero = 0;
     if (!cuda_ok(cudaMemcpyToSymbol(flarepp::g_error_word, &zero, sizeof(zero)), "clear error word"))
       return FLAREPP_ERR_CUDA;
+  }
+  unsigned tc_word = 0;
+  if (!cuda_ok(flarepp::tc_take_error_word(&tc_word), "read tensor-core error word")) return FLAREPP_ERR_CUDA;
+  word |= tc_word;
+  if (word != 0) {
+    snprintf(flarepp::g_last_error, sizeof(flarepp::g_last_error), "device error word 0x%x", word);
     return (word & flarepp::kErrTimeout) ? FLAREPP_ERR_TIMEOUT : FLAREPP_ERR_CUDA;
   }
   return FLAREPP_OK;

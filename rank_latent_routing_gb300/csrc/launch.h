@@ -1,0 +1,54 @@
+// Interface between the host API (flarepp.cu) and the tensor-core kernels
+// (tc.cu): one problem description and the launch entry of each kernel family.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace flarepp {
+
+// One forward call as the kernels see it. All pointers are device pointers.
+struct DeviceProblem {
+  const void* K;       // [BH][N][D]
+  const void* V;       // [BH][N][D]
+  const void* Ks;      // [BH][N][D]
+  const void* Qseed;   // [H][M][D]
+  const void* Qf;      // [H][M][D]
+  const float* gate;   // [H]
+  void* out;           // [BH][N][D]
+  int B, H, N, M, D;
+  float* dbg_qd;       // optional fp32 copies of the intermediate results
+  float* dbg_q;
+  float* dbg_z;
+  float* dbg_l;
+};
+
+// Split-N layout shared by the synthesis and encode passes: `tiles` blocks of
+// 128 latent rows per head, `splits` token ranges of `split_len` tokens (a
+// multiple of 128), and `streams` partial results per (split, row): 2 when
+// M <= 64 (two token streams share one 128-lane tile), else 1.
+struct TcPlan {
+  int tiles, splits, split_len, streams;
+  int decode_ctas_per_head, decode_tiles_per_cta;
+};
+
+// Workspace regions (device pointers into the caller's or the cache's buffer).
+struct TcWorkspace {
+  float* part_z;           // [BH][tiles][splits*streams][128][D]
+  float* part_l;           // [BH][tiles][splits*streams][128]
+  unsigned* counters;      // [2][BH][tiles]
+  void* q;                 // [BH][M][D] bf16 routing queries
+  void* z;                 // [BH][M][D] bf16 latents
+};
+
+TcPlan tc_plan(int B, int H, int N, int M, int D, int sms, int forced_splits);
+// Launches synthesis, encode and decode on `stream`. `events` (4 entries or
+// null) bracket the three passes. Returns a cudaError_t of the first failure.
+cudaError_t tc_forward(const DeviceProblem& p, const TcPlan& pl, const TcWorkspace& ws,
+                       cudaEvent_t* events, cudaStream_t stream, const char** failed_call);
+// Reads and clears the tensor-core kernels' device error word (bit 0: a
+// bounded wait timed out).
+cudaError_t tc_take_error_word(unsigned* word);
+
+}  // namespace flarepp
