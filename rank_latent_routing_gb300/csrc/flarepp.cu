@@ -148,7 +148,7 @@ Plan make_plan(int B, int H, int N, int M, int D, flarepp_dtype_t dtype, int sms
   size_t off = 0;
   pl.off_pz = off; off = align_up(off + rows * D * sizeof(float), 256);
   pl.off_pl = off; off = align_up(off + rows * sizeof(float), 256);
-  pl.off_cnt = off; off = align_up(off + 2 * (size_t)pl.BH * pl.tiles * sizeof(unsigned), 256);
+  pl.off_cnt = off; off = align_up(off + 2 * (size_t)pl.BH * pl.tiles * sizeof(unsigned), 256);  // >= 2 BH qgroups
   const size_t lat = (size_t)pl.BH * M * D * elem_size(dtype);
   pl.off_q = off; off = align_up(off + lat, 256);
   pl.off_z = off; off = align_up(off + lat, 256);

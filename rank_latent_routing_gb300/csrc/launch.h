@@ -25,11 +25,13 @@ struct DeviceProblem {
 };
 
 // Split-N layout shared by the synthesis and encode passes: `tiles` blocks of
-// 128 latent rows per head, `splits` token ranges of `split_len` tokens (a
-// multiple of 128), and `streams` partial results per (split, row): 2 when
-// M <= 64 (two token streams share one 128-lane tile), else 1.
+// (up to) 128 latent rows per head, handled by `qgroups` CTAs per token split
+// (two blocks per CTA when M > 128); `splits` token ranges of `split_len`
+// tokens (a multiple of 128); `streams` partial-result slots per (block,
+// split): 4 when M <= 64, 2 when a block is shared by two token streams, 1 when
+// every block is paired.
 struct TcPlan {
-  int tiles, splits, split_len, streams;
+  int tiles, qgroups, splits, split_len, streams;
   int decode_ctas_per_head, decode_tiles_per_cta;
 };
 

@@ -4,33 +4,37 @@
 // Two kernels carry the three attention calls of the mixer (FLARE++ paper,
 // Section 3.2 eq. 6 and eq. 8):
 //
-//  * split_kernel — a 128-row block of latent queries attends over one token
-//    range (split) of a head: scores S = Qtile * Ktile^T land in TMEM, one
-//    thread per latent row runs an online softmax over the tokens, P goes back
-//    to TMEM in bf16 and the tensor core accumulates O += P * Vtile in TMEM.
-//    The split's (Z_s, L_s) go to global memory and the last CTA of the head to
-//    arrive merges all splits with the stable log-sum-exp schedule of
-//    Appendix B.3 (eq. 29-33). The synthesis instance normalises each staged
-//    Ks_raw tile in place (N0, eq. 5), uses it as both keys and values
-//    (eq. 19) and ends with the gate (eq. 7): Q = N0(Qf) + g * Qd in fp32, cast
-//    to bf16. The encode instance ends with Z (bf16) and L.
-//  * decode_kernel — 128 tokens per tile attend over the M routes: Q and Z of
-//    the head stay in shared memory for all of the CTA's tiles, scores
-//    S = Ktile * Q^T are computed 128 routes at a time, softmax over M per
-//    token (one thread per token), Y += P * Z in TMEM, then Y / l to bf16.
+//  * split_kernel — latent queries attend over one token range (split) of a
+//    head. Scores S = Q K^T land in TMEM; one thread per latent row runs an
+//    online softmax over the tokens; P goes back to TMEM in bf16 over the
+//    scores and the tensor core accumulates O += P [V | 1] in TMEM, the
+//    appended ones column giving the softmax row sum. Each split's (Z_s, L_s)
+//    goes to global memory and the last CTA of a head to arrive merges all
+//    splits with the stable log-sum-exp schedule of Appendix B.3 (eq. 29-33).
+//    The synthesis instance normalises each staged Ks_raw tile in place (N0,
+//    eq. 5), uses it as both keys and values (eq. 19) and ends with the gate
+//    (eq. 7): Q = N0(Qf) + g * Qd in fp32, cast to bf16. The encode instance
+//    ends with Z (bf16) and L.
+//  * decode_kernel — tokens attend over the M routes: Q and Z of the head stay
+//    in shared memory for all of the CTA's token tiles; S = K Q^T is computed
+//    128 routes at a time with an online softmax over M per token, and
+//    O += P [Z | 1]; out = O / rowsum in bf16.
 //
-// Warp roles (256 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues the MMAs (one thread), warps 2-3 normalise synthesis tiles, warps
-// 4-7 run the softmax and the epilogues; warp 4+i reads TMEM lanes 32i..32i+31.
+// One CTA per SM, 384 threads: warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs (one thread), warps 2-3 normalise synthesis tiles, and two
+// softmax warpgroups (warps 4-7 and 8-11) each own one of two TMEM slots, so
+// one slot's softmax runs while the tensor core works on the other's products.
+// Warp w reads TMEM lanes 32*(w%4) .. +31.
 //
 // Every wait on an mbarrier is bounded: after about a second without progress
 // the thread records kErrTimeout in the device error word, raises the CTA's
 // abort flag and leaves its loop, so a broken invariant ends the kernel
 // instead of hanging the GPU.
 #include <cuda.h>
-#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "launch.h"
@@ -43,24 +47,29 @@ using namespace sm100;
 
 __device__ unsigned g_tc_error = 0u;
 
-constexpr int kThreads = 256;
-constexpr int kTile = 128;      // tokens per staged tile; latents per row block
-constexpr int kStages = 4;      // token-tile ring depth
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;    // fp32 scores, 128 columns
-constexpr uint32_t kColP = 128;  // bf16 probabilities, 64 columns (128 packed pairs)
-constexpr uint32_t kColO = 192;  // fp32 output accumulator, D columns
+constexpr int kThreads = 384;
+constexpr int kTile = 128;          // tokens per staged tile; latents per row block
+constexpr int kStages = 6;          // token-tile ring depth
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSlotCols = 256;  // slot s: scores/probabilities at s*256, accumulator at +128
+constexpr uint32_t kColO = 128;
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
-constexpr size_t kMinSmem = 80 * 1024;          // keeps residency at <= 2 CTAs per SM
+
+// How the two TMEM slots of a split-kernel CTA divide the work:
+//  kLanes   (M <= 64)  each slot holds the latents twice; lanes 0-63 and 64-127
+//                      score different token tiles (4 token streams per CTA);
+//  kStreams            one 128-row latent block, the slots take alternate tiles;
+//  kPair               two 128-row latent blocks, both slots see every tile.
+enum : int { kLanes = 0, kStreams = 1, kPair = 2 };
 
 struct Shared {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t norm[kStages];
   uint64_t q_full;
-  uint64_t s_full;
-  uint64_t p_full;
-  uint64_t o_full;
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -75,45 +84,52 @@ __device__ __forceinline__ bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_
   return false;
 }
 
-__device__ __forceinline__ void named_sync_softmax() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
+// Barrier over the two softmax warpgroups only (256 threads).
+__device__ __forceinline__ void softmax_groups_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 template <int D>
 struct Layout {
   static constexpr uint32_t kRowBytes = D * 2;
-  static constexpr uint32_t kAtom = 8 * kRowBytes;          // one swizzle repeat (8 rows)
+  static constexpr uint32_t kAtom = 8 * kRowBytes;           // one swizzle repeat (8 rows)
   static constexpr uint32_t kTileBytes = kTile * kRowBytes;  // 128 rows
   static constexpr uint32_t kSwz = D == 32 ? kSwizzle64 : kSwizzle32;
+  static constexpr int kNo = D + 16;  // accumulator columns: D values, the row sum, padding
   // K-major operand (rows x D), k-th 16-element slice
   static __device__ __forceinline__ uint64_t kmajor(uint32_t base, int k) {
     return sdesc(base + k * 32, 16, kAtom, kSwz);
   }
-  // MN-major operand: rows are the K dimension, D columns the N dimension;
-  // slice kk covers rows 16kk .. 16kk+15
-  static __device__ __forceinline__ uint64_t mnmajor(uint32_t base, int kk) {
-    return sdesc(base + kk * 2 * kAtom, 16, kAtom, kSwz);
+  // MN-major [values | ones] operand: rows are the K dimension; the D value
+  // columns sit at `base`, the ones column block `ones - base` bytes further.
+  // Slice kk covers rows 16kk .. 16kk+15.
+  static __device__ __forceinline__ uint64_t values1(uint32_t base, uint32_t ones, int kk) {
+    return sdesc(base + kk * 2 * kAtom, ones - base, kAtom, kSwz);
+  }
+  // Byte offset of logical 16-byte chunk `c` of row `r` in a swizzled tile.
+  static __device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
+    const int x = D == 32 ? ((r >> 1) & 3) : ((r >> 2) & 1);
+    return r * kRowBytes + ((c ^ x) << 4);
   }
 };
 
-// exp2 of x <= 0 (or slightly above after a lazy max): MUFU ex2.
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+// Fills a 128-row tile, in the swizzled layout of the value tiles, with rows
+// [1, 0, ..., 0]: as the extra column block of an MN-major B operand it makes
+// the MMA add the probabilities of each row into accumulator column D.
+template <int D>
+__device__ void fill_ones(unsigned char* tile, int tid, int nthreads) {
+  using L = Layout<D>;
+  for (int i = tid; i < kTile * (D / 8); i += nthreads) {
+    const int r = i / (D / 8), c = i % (D / 8);
+    const uint4 v = make_uint4(c == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);  // bf16 1.0 in element 0
+    *reinterpret_cast<uint4*>(tile + L::chunk_offset(r, c)) = v;
+  }
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&b);
-}
-
-// Scales the D accumulator columns of this thread's TMEM lane by `alpha`.
+// Scales the accumulator columns (values and row sum) of this lane by `alpha`.
 template <int D>
 __device__ __forceinline__ void rescale_acc(uint32_t taddr, float alpha) {
   uint32_t r[16];
 #pragma unroll
-  for (int c = 0; c < D; c += 16) {
+  for (int c = 0; c < Layout<D>::kNo; c += 16) {
     tmem_ld16(taddr + c, r);
     tmem_wait_ld();
 #pragma unroll
@@ -123,111 +139,76 @@ __device__ __forceinline__ void rescale_acc(uint32_t taddr, float alpha) {
   tmem_wait_st();
 }
 
+// Reads the D output values and the row sum of this lane's accumulator.
 template <int D>
-__device__ __forceinline__ void load_acc(uint32_t taddr, float (&o)[D]) {
-  uint32_t r[16];
-#pragma unroll
-  for (int c = 0; c < D; c += 16) {
-    tmem_ld16(taddr + c, r);
+__device__ __forceinline__ float load_acc(uint32_t taddr, float (&o)[D]) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  if (D == 32) {
+    uint32_t s[16];
+    tmem_ld16(taddr + 32, s);
     tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o[c + i] = __uint_as_float(r[i]);
+    for (int i = 0; i < D; ++i) o[i] = __uint_as_float(r[i]);
+    return __uint_as_float(s[0]);
   }
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < D; ++i) o[i] = __uint_as_float(r[i]);
+  return __uint_as_float(r[D]);
 }
 
-// One softmax step over `width` (multiple of 16, <= 128) score columns of this
-// thread's TMEM lane, columns >= `valid` masked out. Keeps the running max
-// `m` (raw score units) and sum `l`; rescales the accumulator lazily, only
-// when the max grows by more than 2^8 in exp2 units, so p <= 256 always.
-// Writes P (bf16 pairs) to the P columns. `has_acc`: the accumulator holds
-// earlier steps' products.
-template <int D>
-__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tP, uint32_t tO, int width, int valid,
-                                             float c, float& m, float& l, bool has_acc) {
+// One softmax step over `kWidth` (32, 64 or 128) score columns of this lane,
+// columns >= `valid` masked. `m` is the running max in raw score units; it
+// moves only when the tile max exceeds it by more than 2^8 in exp2 units
+// (then the accumulator, row sum included, is rescaled), so p <= 256. P is
+// written in bf16 over the first kWidth/2 score columns. Warp-uniform: every
+// lane of a warp calls it with the same width and valid count.
+template <int D, int kWidth>
+__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int valid, float c, float& m,
+                                             bool has_acc) {
   constexpr float kLazy = 8.0f;
-  float tmax = -INFINITY;
-  for (int base = 0; base < width; base += 32) {
-    uint32_t r[32];
-    if (width - base >= 32) {
-      tmem_ld32(tS + base, r);
-    } else {
-      uint32_t h[16];
-      tmem_ld16(tS + base, h);
+  uint32_t r[kWidth];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) { r[i] = h[i]; r[16 + i] = __float_as_uint(-INFINITY); }
-    }
-    tmem_wait_ld();
-    if (valid - base >= 32) {
+  for (int b = 0; b < kWidth; b += 32) tmem_ld32(tS + b, *reinterpret_cast<uint32_t(*)[32]>(r + b));
+  tmem_wait_ld();
+  if (valid < kWidth) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 2)
-        tmax = fmaxf(tmax, fmaxf(__uint_as_float(r[i]), __uint_as_float(r[i + 1])));
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (base + i < valid) tmax = fmaxf(tmax, __uint_as_float(r[i]));
-    }
+    for (int i = 0; i < kWidth; ++i)
+      if (i >= valid) r[i] = __float_as_uint(-INFINITY);
   }
-  // the max moves only when it grows by more than 2^8 (in exp2 units); TMEM
-  // access is warp-collective, so the warp rescales together (alpha = 1 for
-  // lanes whose max stays)
+  float tmax = m;
+#pragma unroll
+  for (int i = 0; i < kWidth; i += 2) tmax = max3(tmax, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
   const bool grow = tmax > m && (m == -INFINITY || (tmax - m) * c > kLazy);
   float alpha = 1.f;
   if (grow) {
     alpha = m == -INFINITY ? 0.f : ex2((m - tmax) * c);
-    l *= alpha;
     m = tmax;
   }
   if (has_acc && __any_sync(0xFFFFFFFFu, grow)) rescale_acc<D>(tO, alpha);
-  const float mc = m * c;
-  for (int base = 0; base < width; base += 32) {
-    uint32_t r[32];
-    const bool full = width - base >= 32;
-    if (full) {
-      tmem_ld32(tS + base, r);
-    } else {
-      uint32_t h[16];
-      tmem_ld16(tS + base, h);
+  const float2 cc = make_float2(c, c);
+  const float2 mc = make_float2(-m * c, -m * c);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) { r[i] = h[i]; r[16 + i] = 0u; }
-    }
-    tmem_wait_ld();
-    uint32_t pk[16];
-    if (valid - base >= 32) {
+  for (int i = 0; i < kWidth / 2; ++i) {
+    const float2 x = fma2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), cc, mc);
+    r[i] = pack_bf16x2(ex2(x.x), ex2(x.y));
+  }
+  if (kWidth >= 64) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), c, -mc));
-        const float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), c, -mc));
-        l += p0 + p1;
-        pk[i] = pack_bf16(p0, p1);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float p0 = base + 2 * i < valid ? ex2(fmaf(__uint_as_float(r[2 * i]), c, -mc)) : 0.f;
-        const float p1 = base + 2 * i + 1 < valid ? ex2(fmaf(__uint_as_float(r[2 * i + 1]), c, -mc)) : 0.f;
-        l += p0 + p1;
-        pk[i] = pack_bf16(p0, p1);
-      }
-    }
-    if (full) {
-      tmem_st16(tP + base / 2, pk);
-    } else {
-      // 16 score columns -> 8 packed columns
-      uint32_t a[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = pk[i];
-      tmem_st8(tP + base / 2, a);
-    }
+    for (int b = 0; b < kWidth / 2; b += 32) tmem_st32(tS + b, *reinterpret_cast<uint32_t(*)[32]>(r + b));
+  } else {
+    tmem_st16(tS, *reinterpret_cast<uint32_t(*)[16]>(r));
   }
   tmem_wait_st();
 }
 
 // ------------------------------------------------------------ split kernel
 struct SplitParams {
-  int N, M, H, tiles, splits, split_len, streams;
-  float* part_z;
-  float* part_l;
-  unsigned* counters;
+  int N, M, H, qtiles, splits, split_len, pstreams;
+  float* part_z;            // [BH][qtiles][splits][pstreams][128][D]
+  float* part_l;            // [BH][qtiles][splits][pstreams][128]
+  unsigned* counters;       // [BH][qgroups]
   const __nv_bfloat16* qf;  // synthesis: [H][M][D]
   const float* gate;        // synthesis: [H]
   __nv_bfloat16* out;       // synthesis: Q; encode: Z ([BH][M][D])
@@ -235,8 +216,45 @@ struct SplitParams {
   float* dbg_b;             // synthesis: Q (as rounded); encode: L
 };
 
+struct SlotPlan {
+  int mode;
+  int qt[2];     // latent block of each slot
+  int steps[2];  // steps each slot processes
+};
+
+__device__ __forceinline__ SlotPlan slot_plan(int M, int qtiles, int group, int T) {
+  SlotPlan s;
+  if (M <= 64) {
+    s.mode = kLanes;
+    s.qt[0] = s.qt[1] = 0;
+  } else if (2 * group + 1 < qtiles) {
+    s.mode = kPair;
+    s.qt[0] = 2 * group;
+    s.qt[1] = 2 * group + 1;
+  } else {
+    s.mode = kStreams;
+    s.qt[0] = s.qt[1] = 2 * group;
+  }
+  for (int k = 0; k < 2; ++k) {
+    if (s.mode == kLanes) s.steps[k] = T > 2 * k ? (T - 2 * k + 3) / 4 : 0;
+    else if (s.mode == kStreams) s.steps[k] = T > k ? (T - k + 1) / 2 : 0;
+    else s.steps[k] = T;
+  }
+  return s;
+}
+
+// Token tile of slot k at step j (in the lanes mode lanes 64-127 take tile + 1).
+__device__ __forceinline__ int slot_tile(const SlotPlan& s, int k, int j) {
+  if (s.mode == kLanes) return 4 * j + 2 * k;
+  if (s.mode == kStreams) return 2 * j + k;
+  return j;
+}
+
+// Partial results per latent block and split: 4, 2 or 1 token streams.
+__device__ __forceinline__ int block_streams(int mode) { return mode == kLanes ? 4 : (mode == kStreams ? 2 : 1); }
+
 template <int D, bool kSynth>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
   using L = Layout<D>;
@@ -245,18 +263,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   constexpr uint32_t kStageBytes = kSynth ? L::kTileBytes : 2 * L::kTileBytes;
-  unsigned char* sQ = smem;
-  unsigned char* sStage = smem + 8192;
+  unsigned char* sQ = smem;                                   // [2][128][D]
+  unsigned char* sStage = smem + 2 * L::kTileBytes;           // [kStages] x (K, V)
+  unsigned char* sOnes = sStage + kStages * kStageBytes;      // [128][D] rows [1, 0, ...]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int split = blockIdx.x, tile = blockIdx.y, bh = blockIdx.z;
+  const int split = blockIdx.x, group = blockIdx.y, bh = blockIdx.z;
   const int h = bh % p.H;
-  const bool two = p.streams == 2;
   const int n_begin = split * p.split_len;
   const int n_end = min(p.N, n_begin + p.split_len);
-  const int T = n_begin < n_end ? (n_end - n_begin + kTile - 1) / kTile : 0;  // token tiles
-  const int steps = two ? (T + 1) / 2 : T;
+  const int T = n_begin < n_end ? (n_end - n_begin + kTile - 1) / kTile : 0;
+  const SlotPlan sp = slot_plan(p.M, p.qtiles, group, T);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -265,9 +283,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&sh.norm[s], 64);
     }
     mbar_init(&sh.q_full, 1);
-    mbar_init(&sh.s_full, 1);
-    mbar_init(&sh.p_full, 128);
-    mbar_init(&sh.o_full, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&sh.s_full[k], 1);
+      mbar_init(&sh.p_full[k], 128);
+      mbar_init(&sh.o_full[k], 1);
+    }
     mbar_init(&sh.drain, 1);
     sh.abort = 0;
     sh.last = 0;
@@ -277,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     tmem_alloc(&sh.tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  if (warp >= 4) fill_ones<D>(sOnes, threadIdx.x - 128, 256);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -289,13 +311,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       prefetch_tmap(&tm_k);
       if (!kSynth) prefetch_tmap(&tm_v);
       const int qz = kSynth ? h : bh;
-      if (two) {
-        mbar_arrive_expect_tx(&sh.q_full, L::kTileBytes);
+      mbar_arrive_expect_tx(&sh.q_full, (sp.mode == kPair ? 2 : 1) * L::kTileBytes);
+      if (sp.mode == kLanes) {
+        // the 64 (or fewer) latents twice: lanes 64-127 repeat lanes 0-63
         tma_load_3d(sQ, &tm_q, &sh.q_full, 0, 0, qz);
         tma_load_3d(sQ + L::kTileBytes / 2, &tm_q, &sh.q_full, 0, 0, qz);
       } else {
-        mbar_arrive_expect_tx(&sh.q_full, L::kTileBytes);
-        tma_load_3d(sQ, &tm_q, &sh.q_full, 0, tile * kTile, qz);
+        tma_load_3d(sQ, &tm_q, &sh.q_full, 0, sp.qt[0] * kTile, qz);
+        if (sp.mode == kPair) tma_load_3d(sQ + L::kTileBytes, &tm_q, &sh.q_full, 0, sp.qt[1] * kTile, qz);
       }
       int issued = 0;
       for (int t = 0; t < T; ++t) {
@@ -311,76 +334,99 @@ __global__ void __launch_bounds__(kThreads, 2)
         // let the copies still in flight land before the CTA leaves
         for (int t = max(0, issued - kStages); t < issued; ++t)
           mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, kWaitLimit);
+        mbar_wait(&sh.q_full, 0, kWaitLimit);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t aQ = smem_u32(sQ);
+      const uint32_t aQ0 = smem_u32(sQ);
+      const uint32_t aQ1 = sp.mode == kPair ? aQ0 + L::kTileBytes : aQ0;
+      const uint32_t aOnes = smem_u32(sOnes);
       const uint32_t idS = idesc_bf16(128, kTile, false, false);
-      const uint32_t idO = idesc_bf16(128, D, false, true);
-      bool ok = wait_or_abort(sh, &sh.q_full, 0);
-      for (int j = 0; ok && j < steps; ++j) {
-        const int ta = two ? 2 * j : j;
-        const bool has_b = two && (2 * j + 1 < T);
-        const int sa = ta % kStages, sb = (ta + 1) % kStages;
-        uint64_t* ready_a = kSynth ? &sh.norm[sa] : &sh.full[sa];
-        uint64_t* ready_b = kSynth ? &sh.norm[sb] : &sh.full[sb];
-        if (!wait_or_abort(sh, ready_a, (ta / kStages) & 1)) break;
-        if (has_b && !wait_or_abort(sh, ready_b, ((ta + 1) / kStages) & 1)) break;
-        tc_fence_after();
-        const uint32_t kA = smem_u32(sStage + sa * kStageBytes);
-        const uint32_t kB = smem_u32(sStage + sb * kStageBytes);
-        if (!two) {
+      const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
+      constexpr uint32_t kLo = 0u, kAll = 0xFFFFFFFFu;
+      auto stage_addr = [&](int t) { return smem_u32(sStage + (t % kStages) * kStageBytes); };
+      auto ready = [&](int t) -> bool {
+        return wait_or_abort(sh, kSynth ? &sh.norm[t % kStages] : &sh.full[t % kStages], (t / kStages) & 1);
+      };
+      // scores of slot k, step j
+      auto issue_s = [&](int k, int j) -> bool {
+        const uint32_t dS = tmem + k * kSlotCols;
+        const uint32_t aQ = k == 0 ? aQ0 : aQ1;
+        const int t = slot_tile(sp, k, j);
+        if (!ready(t)) return false;
+        if (sp.mode == kLanes) {
+          const bool has_b = t + 1 < T;
+          if (has_b && !ready(t + 1)) return false;
+          tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss(tmem + kColS, L::kmajor(aQ, k), L::kmajor(kA, k), idS, k > 0);
-        } else {
-          // rows 0-63 score the even tile, rows 64-127 (same latents) the odd one
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_masked(tmem + kColS, L::kmajor(aQ, k), L::kmajor(kA, k), idS, k > 0, 0u, 0u,
-                          0xFFFFFFFFu, 0xFFFFFFFFu);
+          for (int q = 0; q < D / 16; ++q)
+            mma_ss_masked(dS, L::kmajor(aQ, q), L::kmajor(stage_addr(t), q), idS, q > 0, kLo, kLo, kAll, kAll);
           if (has_b) {
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k)
-              mma_ss_masked(tmem + kColS, L::kmajor(aQ, k), L::kmajor(kB, k), idS, k > 0, 0xFFFFFFFFu,
-                            0xFFFFFFFFu, 0u, 0u);
+            for (int q = 0; q < D / 16; ++q)
+              mma_ss_masked(dS, L::kmajor(aQ, q), L::kmajor(stage_addr(t + 1), q), idS, q > 0, kAll, kAll, kLo,
+                            kLo);
           }
-        }
-        mma_commit(&sh.s_full);
-        if (!wait_or_abort(sh, &sh.p_full, j & 1)) break;
-        tc_fence_after();
-        const uint32_t vA = kSynth ? kA : kA + L::kTileBytes;
-        const uint32_t vB = kSynth ? kB : kB + L::kTileBytes;
-        if (!two) {
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + kColO, tmem + kColP + kk * 8, L::mnmajor(vA, kk), idO, (j > 0 || kk > 0));
         } else {
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < D / 16; ++q) mma_ss(dS, L::kmajor(aQ, q), L::kmajor(stage_addr(t), q), idS, q > 0);
+        }
+        mma_commit(&sh.s_full[k]);
+        return true;
+      };
+      // O += P [V | 1] for slot k, step j; releases the tiles no longer needed
+      auto issue_pv = [&](int k, int j) {
+        const uint32_t dO = tmem + k * kSlotCols + kColO;
+        const uint32_t aP = tmem + k * kSlotCols;
+        const int t = slot_tile(sp, k, j);
+        const uint32_t vA = stage_addr(t) + (kSynth ? 0 : L::kTileBytes);
+        if (sp.mode == kLanes) {
+          const bool has_b = t + 1 < T;
+          const uint32_t vB = stage_addr(t + 1) + (kSynth ? 0 : L::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts_masked(tmem + kColO, tmem + kColP + kk * 8, L::mnmajor(vA, kk), idO, (j > 0 || kk > 0),
-                          0u, 0u, 0xFFFFFFFFu, 0xFFFFFFFFu);
+            mma_ts_masked(dO, aP + kk * 8, L::values1(vA, aOnes, kk), idO, (j > 0 || kk > 0), kLo, kLo, kAll, kAll);
           if (has_b) {
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ts_masked(tmem + kColO, tmem + kColP + kk * 8, L::mnmajor(vB, kk), idO,
-                            (j > 0 || kk > 0), 0xFFFFFFFFu, 0xFFFFFFFFu, 0u, 0u);
+              mma_ts_masked(dO, aP + kk * 8, L::values1(vB, aOnes, kk), idO, (j > 0 || kk > 0), kAll, kAll, kLo,
+                            kLo);
           }
+          mma_commit(&sh.empty[t % kStages]);
+          if (has_b) mma_commit(&sh.empty[(t + 1) % kStages]);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(dO, aP + kk * 8, L::values1(vA, aOnes, kk), idO, (j > 0 || kk > 0));
+          if (sp.mode == kStreams || k == 1) mma_commit(&sh.empty[t % kStages]);
         }
-        mma_commit(&sh.empty[sa]);
-        if (has_b) mma_commit(&sh.empty[sb]);
+      };
+      bool ok = wait_or_abort(sh, &sh.q_full, 0);
+      for (int k = 0; ok && k < 2; ++k)
+        if (sp.steps[k] > 0) ok = issue_s(k, 0);
+      const int jmax = max(sp.steps[0], sp.steps[1]);
+      for (int j = 0; ok && j < jmax; ++j) {
+        for (int k = 0; ok && k < 2; ++k) {
+          if (j >= sp.steps[k]) continue;
+          if (!wait_or_abort(sh, &sh.p_full[k], j & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(k, j);
+          if (j + 1 < sp.steps[k]) ok = issue_s(k, j + 1);
+        }
       }
-      mma_commit(&sh.o_full);
-      // all MMAs of this CTA complete before TMEM is released
+      mma_commit(&sh.o_full[0]);
+      mma_commit(&sh.o_full[1]);
+      // every MMA of this CTA completes before TMEM is released
       mma_commit(&sh.drain);
       mbar_wait(&sh.drain, 0, kWaitLimit);
     }
   } else if (warp < 4) {
     // ------------------------------------------- N0 of the synthesis tiles
     if (kSynth) {
-      const int nt = threadIdx.x - 64;  // 0..63, rows nt and nt + 64
+      const int nt = threadIdx.x - 64;  // 0..63: rows nt and nt + 64 of each tile
       for (int t = 0; t < T; ++t) {
         const int s = t % kStages;
         if (!wait_or_abort(sh, &sh.full[s], (t / kStages) & 1)) break;
@@ -395,8 +441,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             v[i] = row[i];
             const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
+            for (int q = 0; q < 4; ++q) {
+              const float a = __uint_as_float(w[q] << 16), b = __uint_as_float(w[q] & 0xFFFF0000u);
               ss = fmaf(a, a, fmaf(b, b, ss));
             }
           }
@@ -405,8 +451,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int i = 0; i < D / 8; ++i) {
             uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              w[j] = pack_bf16(__uint_as_float(w[j] << 16) * r, __uint_as_float(w[j] & 0xFFFF0000u) * r);
+            for (int q = 0; q < 4; ++q)
+              w[q] = pack_bf16x2(__uint_as_float(w[q] << 16) * r, __uint_as_float(w[q] & 0xFFFF0000u) * r);
             row[i] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
@@ -416,82 +462,88 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
-    const int row = threadIdx.x - 128;
+    const int k = (warp - 4) >> 2;  // slot
+    const int row = (threadIdx.x - 128) & 127;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t tS = tmem + lane_base + kColS;
-    const uint32_t tP = tmem + lane_base + kColP;
-    const uint32_t tO = tmem + lane_base + kColO;
-    const int stream = two ? (row >> 6) : 0;
-    const int r_in = two ? (row & 63) : row;
-    const int latent = tile * kTile + r_in;
+    const uint32_t tS = tmem + lane_base + k * kSlotCols;
+    const uint32_t tO = tS + kColO;
+    const int half = sp.mode == kLanes ? (row >> 6) : 0;
+    const int r_in = sp.mode == kLanes ? (row & 63) : row;
+    const int qt = sp.qt[k];
+    const int latent = qt * kTile + r_in;
     const bool valid = latent < p.M;
     const float c = rsqrtf((float)D) * kLog2e;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY;
     bool has_acc = false;
     bool ok = true;
-    for (int j = 0; j < steps; ++j) {
-      if (!wait_or_abort(sh, &sh.s_full, j & 1)) { ok = false; break; }
+    for (int j = 0; j < sp.steps[k]; ++j) {
+      if (!wait_or_abort(sh, &sh.s_full[k], j & 1)) { ok = false; break; }
       tc_fence_after();
-      const int t = two ? 2 * j + stream : j;
+      const int t = slot_tile(sp, k, j) + half;
       if (t < T) {
         const int n0 = n_begin + t * kTile;
-        softmax_step<D>(tS, tP, tO, kTile, min(kTile, n_end - n0), c, m, l, has_acc);
+        softmax_step<D, kTile>(tS, tO, min(kTile, n_end - n0), c, m, has_acc);
         has_acc = true;
       }
-      // (a stream with no tile in the last step skips it: its lanes of the
-      // two masked products are neither computed into S nor accumulated)
       tc_fence_before();
-      mbar_arrive(&sh.p_full);
+      mbar_arrive(&sh.p_full[k]);
     }
-    if (ok) ok = wait_or_abort(sh, &sh.o_full, 0);
+    if (ok) ok = wait_or_abort(sh, &sh.o_full[k], 0);
     tc_fence_after();
     float o[D];
-    load_acc<D>(tO, o);
-    const int streams_total = p.splits * p.streams;
-    const size_t grp = (size_t)bh * p.tiles + tile;
+    const float l = load_acc<D>(tO, o);
+    const int nstreams = block_streams(sp.mode);
+    const int stream = sp.mode == kLanes ? 2 * k + half : (sp.mode == kStreams ? k : 0);
+    const size_t blk = (size_t)bh * p.qtiles + qt;
     if (valid) {
-      const size_t prow = (grp * streams_total + (size_t)split * p.streams + stream) * kTile + r_in;
-      float z[D];
-      const bool any = ok && l > 0.f;  // a stream with no token never wrote its accumulator
+      const size_t prow = ((blk * p.splits + split) * p.pstreams + stream) * kTile + r_in;
+      const bool any = ok && has_acc && l > 0.f;  // a stream with no token never wrote its accumulator
       const float inv = any ? 1.f / l : 0.f;
+      float z[D];
 #pragma unroll
       for (int d = 0; d < D; ++d) z[d] = any ? o[d] * inv : 0.f;
       store_row<D>(p.part_z + prow * D, z);
       p.part_l[prow] = any ? (m * c + __log2f(l)) * kLn2 : -INFINITY;
     }
     __threadfence();
-    named_sync_softmax();
-    if (row == 0) {
+    softmax_groups_sync();
+    const size_t grp = (size_t)bh * gridDim.y + group;
+    if (threadIdx.x == 128) {
       const unsigned prev = atomicAdd(p.counters + grp, 1u);
       sh.last = prev == (unsigned)(p.splits - 1);
     }
-    named_sync_softmax();
+    softmax_groups_sync();
     if (sh.last) {
       __threadfence();
-      if (row == 0) p.counters[grp] = 0u;  // ready for the next call
-      const bool merges = valid && (!two || row < 64);
+      if (threadIdx.x == 128) p.counters[grp] = 0u;  // ready for the next call
+      // each latent row of the group is merged once: by slot 0, and by slot 1
+      // for the second block of a pair
+      const bool merges = valid && (k == 0 || sp.mode == kPair) && (sp.mode != kLanes || row < 64);
       if (merges) {
         // Appendix B.3: L_max, d_s = exp(L_s - L_max), U = sum d_s Z_s, Z = U / d
-        const size_t p0 = grp * streams_total * kTile + r_in;
         float lmax = -INFINITY;
-        for (int s = 0; s < streams_total; ++s) lmax = fmaxf(lmax, __ldcg(p.part_l + p0 + (size_t)s * kTile));
+        for (int s = 0; s < p.splits; ++s)
+          for (int q = 0; q < nstreams; ++q)
+            lmax = fmaxf(lmax, __ldcg(p.part_l + ((blk * p.splits + s) * p.pstreams + q) * kTile + r_in));
         float u[D], dsum = 0.f;
 #pragma unroll
         for (int d = 0; d < D; ++d) u[d] = 0.f;
-        for (int s = 0; s < streams_total; ++s) {
-          const size_t r = p0 + (size_t)s * kTile;
-          const float ls = __ldcg(p.part_l + r);
-          if (ls == -INFINITY) continue;
-          const float w = __expf(ls - lmax);
-          dsum += w;
-          const float4* zr = reinterpret_cast<const float4*>(p.part_z + r * D);
+        for (int s = 0; s < p.splits; ++s) {
+          for (int q = 0; q < nstreams; ++q) {
+            const size_t r = ((blk * p.splits + s) * p.pstreams + q) * kTile + r_in;
+            const float ls = __ldcg(p.part_l + r);
+            if (ls == -INFINITY) continue;
+            const float w = __expf(ls - lmax);
+            dsum += w;
+            const float4* zr = reinterpret_cast<const float4*>(p.part_z + r * D);
 #pragma unroll
-          for (int d = 0; d < D; d += 4) {
-            const float4 zz = __ldcg(zr + d / 4);
-            u[d] = fmaf(w, zz.x, u[d]);
-            u[d + 1] = fmaf(w, zz.y, u[d + 1]);
-            u[d + 2] = fmaf(w, zz.z, u[d + 2]);
-            u[d + 3] = fmaf(w, zz.w, u[d + 3]);
+            for (int d = 0; d < D; d += 4) {
+              const float4 zz = __ldcg(zr + d / 4);
+              u[d] = fmaf(w, zz.x, u[d]);
+              u[d + 1] = fmaf(w, zz.y, u[d + 1]);
+              u[d + 2] = fmaf(w, zz.z, u[d + 2]);
+              u[d + 3] = fmaf(w, zz.w, u[d + 3]);
+            }
           }
         }
         const float invd = 1.f / dsum;
@@ -542,7 +594,7 @@ struct DecodeParams {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_z, const DecodeParams p) {
   using L = Layout<D>;
@@ -554,6 +606,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned char* sQ = smem;                                // [chunks][128][D]
   unsigned char* sZ = smem + chunks * L::kTileBytes;       // [chunks][128][D]
   unsigned char* sK = smem + 2 * chunks * L::kTileBytes;   // [kStages][128][D]
+  unsigned char* sOnes = sK + kStages * L::kTileBytes;     // [128][D]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -561,6 +614,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int n_tiles = (p.N + kTile - 1) / kTile;
   const int t_begin = blockIdx.x * p.tiles_per_cta;
   const int T = max(0, min(n_tiles, t_begin + p.tiles_per_cta) - t_begin);
+  // slot k takes local tiles k, k+2, ...; each tile runs `chunks` route blocks
+  int steps[2];
+  for (int k = 0; k < 2; ++k) steps[k] = T > k ? ((T - k + 1) / 2) * chunks : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -568,9 +624,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&sh.empty[s], 1);
     }
     mbar_init(&sh.q_full, 1);
-    mbar_init(&sh.s_full, 1);
-    mbar_init(&sh.p_full, 128);
-    mbar_init(&sh.o_full, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&sh.s_full[k], 1);
+      mbar_init(&sh.p_full[k], 128);
+      mbar_init(&sh.o_full[k], 1);
+    }
     mbar_init(&sh.drain, 1);
     sh.abort = 0;
     fence_mbar_init();
@@ -579,6 +637,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     tmem_alloc(&sh.tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  if (warp >= 4) fill_ones<D>(sOnes, threadIdx.x - 128, 256);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -610,66 +670,85 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t aQ = smem_u32(sQ), aZ = smem_u32(sZ);
-      const uint32_t idO = idesc_bf16(128, D, false, true);
-      bool ok = wait_or_abort(sh, &sh.q_full, 0);
-      int step = 0;
-      for (int t = 0; ok && t < T; ++t) {
+      const uint32_t aQ = smem_u32(sQ), aZ = smem_u32(sZ), aOnes = smem_u32(sOnes);
+      const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
+      // step u of slot k: local tile k + 2*(u / chunks), route block u % chunks
+      auto issue_s = [&](int k, int u) -> bool {
+        const int t = k + 2 * (u / chunks), ch = u % chunks;
         const int s = t % kStages;
-        if (!wait_or_abort(sh, &sh.full[s], (t / kStages) & 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t aK = smem_u32(sK + s * L::kTileBytes);
-        for (int ch = 0; ch < chunks; ++ch, ++step) {
-          const int width = min(kTile, p.M - ch * kTile);
-          const uint32_t idS = idesc_bf16(128, width, false, false);
-          const uint32_t qc = aQ + ch * L::kTileBytes;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) mma_ss(tmem + kColS, L::kmajor(aK, k), L::kmajor(qc, k), idS, k > 0);
-          if (ch == chunks - 1) mma_commit(&sh.empty[s]);
-          mma_commit(&sh.s_full);
-          if (!wait_or_abort(sh, &sh.p_full, step & 1)) { ok = false; break; }
+        if (ch == 0) {
+          if (!wait_or_abort(sh, &sh.full[s], (t / kStages) & 1)) return false;
           tc_fence_after();
-          const uint32_t zc = aZ + ch * L::kTileBytes;
-          for (int kk = 0; kk < width / 16; ++kk)
-            mma_ts(tmem + kColO, tmem + kColP + kk * 8, L::mnmajor(zc, kk), idO, (ch > 0 || kk > 0));
-          if (ch == chunks - 1) mma_commit(&sh.o_full);
+        }
+        const int width = min(kTile, p.M - ch * kTile);
+        const uint32_t aK = smem_u32(sK + s * L::kTileBytes);
+#pragma unroll
+        for (int q = 0; q < D / 16; ++q)
+          mma_ss(tmem + k * kSlotCols, L::kmajor(aK, q), L::kmajor(aQ + ch * L::kTileBytes, q),
+                 idesc_bf16(128, width, false, false), q > 0);
+        if (ch == chunks - 1) mma_commit(&sh.empty[s]);
+        mma_commit(&sh.s_full[k]);
+        return true;
+      };
+      auto issue_pv = [&](int k, int u) {
+        const int ch = u % chunks;
+        const int width = min(kTile, p.M - ch * kTile);
+        const uint32_t zc = aZ + ch * L::kTileBytes;
+        for (int kk = 0; kk < width / 16; ++kk)
+          mma_ts(tmem + k * kSlotCols + kColO, tmem + k * kSlotCols + kk * 8, L::values1(zc, aOnes, kk), idO,
+                 (ch > 0 || kk > 0));
+        if (ch == chunks - 1) mma_commit(&sh.o_full[k]);
+      };
+      bool ok = wait_or_abort(sh, &sh.q_full, 0);
+      for (int k = 0; ok && k < 2; ++k)
+        if (steps[k] > 0) ok = issue_s(k, 0);
+      const int umax = max(steps[0], steps[1]);
+      for (int u = 0; ok && u < umax; ++u) {
+        for (int k = 0; ok && k < 2; ++k) {
+          if (u >= steps[k]) continue;
+          if (!wait_or_abort(sh, &sh.p_full[k], u & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(k, u);
+          if (u + 1 < steps[k]) ok = issue_s(k, u + 1);
         }
       }
       mma_commit(&sh.drain);
       mbar_wait(&sh.drain, 0, kWaitLimit);
     }
   } else if (warp >= 4) {
-    const int row = threadIdx.x - 128;
+    const int k = (warp - 4) >> 2;
+    const int row = (threadIdx.x - 128) & 127;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t tS = tmem + lane_base + kColS;
-    const uint32_t tP = tmem + lane_base + kColP;
-    const uint32_t tO = tmem + lane_base + kColO;
+    const uint32_t tS = tmem + lane_base + k * kSlotCols;
+    const uint32_t tO = tS + kColO;
     const float c = rsqrtf((float)D) * kLog2e;
-    int step = 0;
-    for (int t = 0; t < T; ++t) {
-      float m = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int ch = 0; ch < chunks; ++ch, ++step) {
-        if (!wait_or_abort(sh, &sh.s_full, step & 1)) { ok = false; break; }
-        tc_fence_after();
-        const int width = min(kTile, p.M - ch * kTile);
-        softmax_step<D>(tS, tP, tO, width, width, c, m, l, ch > 0);
-        tc_fence_before();
-        mbar_arrive(&sh.p_full);
-      }
-      if (!ok) break;
-      if (!wait_or_abort(sh, &sh.o_full, t & 1)) break;
+    float m = -INFINITY;
+    for (int u = 0; u < steps[k]; ++u) {
+      const int ch = u % chunks;
+      if (!wait_or_abort(sh, &sh.s_full[k], u & 1)) break;
       tc_fence_after();
-      float y[D];
-      load_acc<D>(tO, y);
-      const int n = (t_begin + t) * kTile + row;
-      if (n < p.N) {
-        const float inv = 1.f / l;
-#pragma unroll
-        for (int d = 0; d < D; ++d) y[d] *= inv;
-        store_row<D>(p.out + ((size_t)bh * p.N + n) * D, y);
-      }
+      if (ch == 0) m = -INFINITY;
+      const int width = min(kTile, p.M - ch * kTile);
+      if (width > 64) softmax_step<D, kTile>(tS, tO, width, c, m, ch > 0);
+      else if (width > 32) softmax_step<D, 64>(tS, tO, width, c, m, ch > 0);
+      else softmax_step<D, 32>(tS, tO, width, c, m, ch > 0);
       tc_fence_before();
+      mbar_arrive(&sh.p_full[k]);
+      if (ch == chunks - 1) {
+        const int t = k + 2 * (u / chunks);
+        if (!wait_or_abort(sh, &sh.o_full[k], (u / chunks) & 1)) break;
+        tc_fence_after();
+        float y[D];
+        const float l = load_acc<D>(tO, y);
+        const int n = (t_begin + t) * kTile + row;
+        if (n < p.N) {
+          const float inv = 1.f / l;
+#pragma unroll
+          for (int d = 0; d < D; ++d) y[d] *= inv;
+          store_row<D>(p.out + ((size_t)bh * p.N + n) * D, y);
+        }
+        tc_fence_before();
+      }
     }
   }
   tc_fence_before();
@@ -716,15 +795,13 @@ bool make_map(CUtensorMap* map, const void* base, int D, int rows, int planes, i
 template <int D>
 size_t split_smem(bool synth) {
   const size_t stage = synth ? Layout<D>::kTileBytes : 2 * Layout<D>::kTileBytes;
-  const size_t need = 1024 + 8192 + kStages * stage;
-  return need < kMinSmem ? kMinSmem : need;
+  return 1024 + 3 * (size_t)Layout<D>::kTileBytes + kStages * stage;
 }
 
 template <int D>
 size_t decode_smem(int M) {
   const int chunks = (M + kTile - 1) / kTile;
-  const size_t need = 1024 + (2 * chunks + kStages) * (size_t)Layout<D>::kTileBytes;
-  return need < kMinSmem ? kMinSmem : need;
+  return 1024 + (2 * chunks + kStages + 1) * (size_t)Layout<D>::kTileBytes;
 }
 
 template <int D>
@@ -733,7 +810,7 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
   const int BH = pr.B * pr.H;
   cudaError_t e;
   CUtensorMap m_seed, m_ks, m_qbuf, m_k, m_v, m_qdec, m_zdec;
-  const int qbox = pl.streams == 2 ? 64 : kTile;
+  const int qbox = pr.M <= 64 ? 64 : kTile;
   *failed = "cuTensorMapEncodeTiled";
   if (!make_map(&m_seed, pr.Qseed, D, pr.M, pr.H, qbox) || !make_map(&m_ks, pr.Ks, D, pr.N, BH, kTile) ||
       !make_map(&m_qbuf, ws.q, D, pr.M, BH, qbox) || !make_map(&m_k, pr.K, D, pr.N, BH, kTile) ||
@@ -741,10 +818,10 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
       !make_map(&m_zdec, ws.z, D, pr.M, BH, kTile))
     return cudaErrorInvalidValue;
 
-  const dim3 grid(pl.splits, pl.tiles, BH);
+  const dim3 grid(pl.splits, pl.qgroups, BH);
   SplitParams sp{};
   sp.N = pr.N; sp.M = pr.M; sp.H = pr.H;
-  sp.tiles = pl.tiles; sp.splits = pl.splits; sp.split_len = pl.split_len; sp.streams = pl.streams;
+  sp.qtiles = pl.tiles; sp.splits = pl.splits; sp.split_len = pl.split_len; sp.pstreams = pl.streams;
   sp.part_z = ws.part_z; sp.part_l = ws.part_l;
 
   if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) { *failed = "cudaEventRecord"; return e; }
@@ -770,7 +847,7 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
   // encode (a4-a5)
   {
     SplitParams a = sp;
-    a.counters = ws.counters + (size_t)BH * pl.tiles;
+    a.counters = ws.counters + (size_t)BH * pl.qgroups;
     a.out = static_cast<__nv_bfloat16*>(ws.z);
     a.dbg_a = pr.dbg_z;
     a.dbg_b = pr.dbg_l;
@@ -803,33 +880,45 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
   return cudaSuccess;
 }
 
+// The split count (per latent group) that fills the SMs best with one CTA
+// per SM: highest fraction of busy SM-waves, fewer splits unless the gain is
+// over 2%, each split at least `min_tiles` token tiles long.
+int choose_splits(long long groups, int n_tiles, int sms, int min_tiles, int forced) {
+  if (forced > 0) return std::min(forced, std::max(1, n_tiles));
+  const int max_splits = std::max(1, n_tiles / std::max(1, min_tiles));
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= std::min(max_splits, 1024); ++s) {
+    const long long units = groups * s;
+    const long long waves = (units + sms - 1) / sms;
+    if (waves > 8) break;
+    const double eff = (double)units / (double)(waves * sms);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
 }  // namespace tc
 
 TcPlan tc_plan(int B, int H, int N, int M, int D, int sms, int forced_splits) {
   (void)D;
   TcPlan pl{};
   const long long BH = (long long)B * H;
-  pl.streams = M <= 64 ? 2 : 1;
-  pl.tiles = pl.streams == 2 ? 1 : (M + tc::kTile - 1) / tc::kTile;
   const int n_tiles = (N + tc::kTile - 1) / tc::kTile;
-  // about two CTAs per SM for each split-N pass, each split a whole number of
-  // token tiles (an even number in the two-stream mode)
-  const int quantum = pl.streams;  // tiles per split step
-  int splits = forced_splits;
-  if (splits <= 0) {
-    const long long groups = BH * pl.tiles;
-    splits = (int)std::min<long long>(256, std::max<long long>(1, (2LL * sms + groups - 1) / groups));
-  }
-  const int max_splits = std::max(1, (n_tiles + quantum - 1) / quantum);
-  splits = std::min(splits, max_splits);
-  int tiles_per_split = (n_tiles + splits - 1) / splits;
-  tiles_per_split = (tiles_per_split + quantum - 1) / quantum * quantum;
+  pl.tiles = M <= 64 ? 1 : (M + tc::kTile - 1) / tc::kTile;
+  pl.qgroups = M <= 128 ? 1 : (pl.tiles + 1) / 2;
+  pl.streams = M <= 64 ? 4 : ((M <= 128 || pl.tiles % 2 == 1) ? 2 : 1);
+  // token tiles per split: at least 4 (two per slot) when the sequence allows
+  const int splits = tc::choose_splits(BH * pl.qgroups, n_tiles, std::max(1, sms), 4, forced_splits);
+  const int tiles_per_split = (n_tiles + splits - 1) / splits;
   pl.split_len = tiles_per_split * tc::kTile;
   pl.splits = (N + pl.split_len - 1) / pl.split_len;
-  // decode: enough CTAs for two per SM, each reusing the head's Q and Z over
-  // consecutive token tiles
-  const long long want = std::max<long long>(1, (2LL * sms + BH - 1) / BH);
-  const int per = (int)std::max<long long>(1, (n_tiles + want - 1) / want);
+  // decode: one CTA per SM over consecutive token tiles of one head
+  const int dsplit = tc::choose_splits(BH, n_tiles, std::max(1, sms), 2, 0);
+  const int per = (n_tiles + dsplit - 1) / dsplit;
   pl.decode_tiles_per_cta = per;
   pl.decode_ctas_per_head = (n_tiles + per - 1) / per;
   return pl;
