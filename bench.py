@@ -43,7 +43,9 @@ UNIT = "tokens/s"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "sm_max_mhz": 2070.0}
 SMS = 152
-MUFU_EX2_PER_CLK_PER_SM = 16  # special-function unit exp2 results per clock per SM
+# exp2 results per clock per SM on the special-function unit: 32 on GB300
+# (measured by python -m rank_latent_routing_gb300.micro; twice B200's 16)
+MUFU_EX2_PER_CLK_PER_SM = 32
 
 
 def load_peaks():
@@ -150,7 +152,7 @@ def roofline(costs, stage_ms, peaks, peak_kind, clock_mhz):
     """The dominant pass against the resource that bounds it.
 
     Ideal times: bytes / HBM peak, flops / bf16 tensor peak, exps / MUFU exp2
-    peak (16 per clock per SM x 152 SMs x the max SM clock). The bound is the
+    peak (32 per clock per SM x 152 SMs x the max SM clock). The bound is the
     resource with the longest ideal time; frac = that ideal time / measured.
     """
     name = max(stage_ms, key=lambda k: stage_ms[k])
@@ -169,7 +171,7 @@ def roofline(costs, stage_ms, peaks, peak_kind, clock_mhz):
         ach, pk, unit = c["exps"] / t / 1e9, exp_peak / 1e9, "Gexp/s"
     return {"bound": bound, "kernel": name, "achieved": round(ach, 3), "peak": round(pk, 3),
             "unit": unit, "frac": round(ach / pk, 4), "traffic": None,
-            "peak_source": peak_kind + (" (MUFU exp2 peak derived from 16/clk/SM x 152 SMs x max "
+            "peak_source": peak_kind + (" (MUFU exp2 peak: measured 32/clk/SM x 152 SMs x max "
                                         "SM clock)" if bound == "alu" else ""),
             "ideal_us": {k: round(v * 1e6, 3) for k, v in ideal.items()},
             "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
