@@ -27,9 +27,8 @@ struct DeviceProblem {
 // Split-N layout shared by the synthesis and encode passes: `tiles` blocks of
 // (up to) 128 latent rows per head, handled by `qgroups` CTAs per token split
 // (two blocks per CTA when M > 128); `splits` token ranges of `split_len`
-// tokens (a multiple of 128); `streams` partial-result slots per (block,
-// split): 4 when M <= 64, 2 when a block is shared by two token streams, 1 when
-// every block is paired.
+// tokens (a multiple of 128); `streams` partial results per (block, split,
+// row): 1, the token streams inside a CTA being merged before the write.
 struct TcPlan {
   int tiles, qgroups, splits, split_len, streams;
   int decode_ctas_per_head, decode_tiles_per_cta;
@@ -37,8 +36,8 @@ struct TcPlan {
 
 // Workspace regions (device pointers into the caller's or the cache's buffer).
 struct TcWorkspace {
-  float* part_z;           // [BH][tiles][splits*streams][128][D]
-  float* part_l;           // [BH][tiles][splits*streams][128]
+  float* part_z;           // [BH][tiles][splits][128][D]
+  float* part_l;           // [BH][tiles][splits][128]
   unsigned* counters;      // [2][BH][tiles]
   void* q;                 // [BH][M][D] bf16 routing queries
   void* z;                 // [BH][M][D] bf16 latents

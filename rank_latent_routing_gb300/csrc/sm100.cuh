@@ -179,6 +179,19 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------- register budget
+// Moves registers between the warpgroups of a CTA: every warp of a warpgroup
+// executes the same call; the counts of all warpgroups must add up to at
+// most the CTA's launch allocation.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ------------------------------------------------------------ packed math
 // d = a * b + c on two fp32 lanes at once (one issue slot for two FMAs).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {

@@ -51,8 +51,9 @@ constexpr int kThreads = 384;
 constexpr int kTile = 128;          // tokens per staged tile; latents per row block
 constexpr int kStages = 6;          // token-tile ring depth
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSlotCols = 256;  // slot s: scores/probabilities at s*256, accumulator at +128
+constexpr uint32_t kSlotCols = 256;  // slot s: scores at s*256, accumulator at +128, probabilities at +176
 constexpr uint32_t kColO = 128;
+constexpr uint32_t kColP = 176;
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
 
 // How the two TMEM slots of a split-kernel CTA divide the work:
@@ -162,24 +163,30 @@ __device__ __forceinline__ float load_acc(uint32_t taddr, float (&o)[D]) {
 // columns >= `valid` masked. `m` is the running max in raw score units; it
 // moves only when the tile max exceeds it by more than 2^8 in exp2 units
 // (then the accumulator, row sum included, is rescaled), so p <= 256. P is
-// written in bf16 over the first kWidth/2 score columns. Warp-uniform: every
-// lane of a warp calls it with the same width and valid count.
+// written in bf16 to the kWidth/2 probability columns at tP. The scores are
+// read twice (max, then exponentials), 64 columns at a time, to keep the
+// live registers low. Warp-uniform: every lane of a warp calls it with the
+// same width and valid count.
 template <int D, int kWidth>
-__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int valid, float c, float& m,
-                                             bool has_acc) {
+__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tP, uint32_t tO, int valid, float c,
+                                             float& m, bool has_acc) {
   constexpr float kLazy = 8.0f;
-  uint32_t r[kWidth];
-#pragma unroll
-  for (int b = 0; b < kWidth; b += 32) tmem_ld32(tS + b, *reinterpret_cast<uint32_t(*)[32]>(r + b));
-  tmem_wait_ld();
-  if (valid < kWidth) {
-#pragma unroll
-    for (int i = 0; i < kWidth; ++i)
-      if (i >= valid) r[i] = __float_as_uint(-INFINITY);
-  }
+  constexpr int kPart = kWidth < 64 ? kWidth : 64;
   float tmax = m;
 #pragma unroll
-  for (int i = 0; i < kWidth; i += 2) tmax = max3(tmax, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+  for (int base = 0; base < kWidth; base += kPart) {
+    uint32_t r[kPart];
+#pragma unroll
+    for (int b = 0; b < kPart; b += 32) tmem_ld32(tS + base + b, *reinterpret_cast<uint32_t(*)[32]>(r + b));
+    tmem_wait_ld();
+    if (valid < base + kPart) {
+#pragma unroll
+      for (int i = 0; i < kPart; ++i)
+        if (base + i >= valid) r[i] = __float_as_uint(-INFINITY);
+    }
+#pragma unroll
+    for (int i = 0; i < kPart; i += 2) tmax = max3(tmax, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+  }
   const bool grow = tmax > m && (m == -INFINITY || (tmax - m) * c > kLazy);
   float alpha = 1.f;
   if (grow) {
@@ -190,24 +197,32 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int valid
   const float2 cc = make_float2(c, c);
   const float2 mc = make_float2(-m * c, -m * c);
 #pragma unroll
-  for (int i = 0; i < kWidth / 2; ++i) {
-    const float2 x = fma2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), cc, mc);
-    r[i] = pack_bf16x2(ex2(x.x), ex2(x.y));
-  }
-  if (kWidth >= 64) {
+  for (int base = 0; base < kWidth; base += kPart) {
+    uint32_t r[kPart];
 #pragma unroll
-    for (int b = 0; b < kWidth / 2; b += 32) tmem_st32(tS + b, *reinterpret_cast<uint32_t(*)[32]>(r + b));
-  } else {
-    tmem_st16(tS, *reinterpret_cast<uint32_t(*)[16]>(r));
+    for (int b = 0; b < kPart; b += 32) tmem_ld32(tS + base + b, *reinterpret_cast<uint32_t(*)[32]>(r + b));
+    tmem_wait_ld();
+    if (valid < base + kPart) {
+#pragma unroll
+      for (int i = 0; i < kPart; ++i)
+        if (base + i >= valid) r[i] = __float_as_uint(-INFINITY);
+    }
+#pragma unroll
+    for (int i = 0; i < kPart / 2; ++i) {
+      const float2 x = fma2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), cc, mc);
+      r[i] = pack_bf16x2(ex2(x.x), ex2(x.y));
+    }
+    if (kPart == 64) tmem_st32(tP + base / 2, *reinterpret_cast<uint32_t(*)[32]>(r));
+    else tmem_st16(tP + base / 2, *reinterpret_cast<uint32_t(*)[16]>(r));
   }
   tmem_wait_st();
 }
 
 // ------------------------------------------------------------ split kernel
 struct SplitParams {
-  int N, M, H, qtiles, splits, split_len, pstreams;
-  float* part_z;            // [BH][qtiles][splits][pstreams][128][D]
-  float* part_l;            // [BH][qtiles][splits][pstreams][128]
+  int N, M, H, qtiles, splits, split_len;
+  float* part_z;            // [BH][qtiles][splits][128][D]
+  float* part_l;            // [BH][qtiles][splits][128]
   unsigned* counters;       // [BH][qgroups]
   const __nv_bfloat16* qf;  // synthesis: [H][M][D]
   const float* gate;        // synthesis: [H]
@@ -249,9 +264,6 @@ __device__ __forceinline__ int slot_tile(const SlotPlan& s, int k, int j) {
   if (s.mode == kStreams) return 2 * j + k;
   return j;
 }
-
-// Partial results per latent block and split: 4, 2 or 1 token streams.
-__device__ __forceinline__ int block_streams(int mode) { return mode == kLanes ? 4 : (mode == kStreams ? 2 : 1); }
 
 template <int D, bool kSynth>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -380,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O += P [V | 1] for slot k, step j; releases the tiles no longer needed
       auto issue_pv = [&](int k, int j) {
         const uint32_t dO = tmem + k * kSlotCols + kColO;
-        const uint32_t aP = tmem + k * kSlotCols;
+        const uint32_t aP = tmem + k * kSlotCols + kColP;
         const int t = slot_tile(sp, k, j);
         const uint32_t vA = stage_addr(t) + (kSynth ? 0 : L::kTileBytes);
         if (sp.mode == kLanes) {
@@ -482,28 +494,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = slot_tile(sp, k, j) + half;
       if (t < T) {
         const int n0 = n_begin + t * kTile;
-        softmax_step<D, kTile>(tS, tO, min(kTile, n_end - n0), c, m, has_acc);
+        softmax_step<D, kTile>(tS, tS + kColP, tO, min(kTile, n_end - n0), c, m, has_acc);
         has_acc = true;
       }
       tc_fence_before();
       mbar_arrive(&sh.p_full[k]);
     }
+    // both slots' products are complete before the stage buffers are reused
+    // as scratch below
     if (ok) ok = wait_or_abort(sh, &sh.o_full[k], 0);
+    if (ok) ok = wait_or_abort(sh, &sh.o_full[k ^ 1], 0);
     tc_fence_after();
     float o[D];
     const float l = load_acc<D>(tO, o);
-    const int nstreams = block_streams(sp.mode);
-    const int stream = sp.mode == kLanes ? 2 * k + half : (sp.mode == kStreams ? k : 0);
-    const size_t blk = (size_t)bh * p.qtiles + qt;
-    if (valid) {
-      const size_t prow = ((blk * p.splits + split) * p.pstreams + stream) * kTile + r_in;
+    (void)valid;
+
+    // 1) each token stream's (L, Z) into shared memory
+    constexpr int kZs = D + 1;  // padded row stride
+    float* scr_l = reinterpret_cast<float*>(sStage);  // [256]
+    float* scr_z = scr_l + 256;                       // [256][D + 1]
+    const int e = threadIdx.x - 128;
+    {
       const bool any = ok && has_acc && l > 0.f;  // a stream with no token never wrote its accumulator
       const float inv = any ? 1.f / l : 0.f;
-      float z[D];
+      scr_l[e] = any ? (m * c + __log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll
-      for (int d = 0; d < D; ++d) z[d] = any ? o[d] * inv : 0.f;
-      store_row<D>(p.part_z + prow * D, z);
-      p.part_l[prow] = any ? (m * c + __log2f(l)) * kLn2 : -INFINITY;
+      for (int d = 0; d < D; ++d) scr_z[e * kZs + d] = any ? o[d] * inv : 0.f;
+    }
+    softmax_groups_sync();
+
+    // 2) one partial result per (latent row, split): the CTA's token streams of
+    //    a row merged first (Appendix B.3 schedule over the streams)
+    {
+      int nent = 1, stride = 0, r_w = row, qt_w = sp.qt[k];
+      bool writer = true;
+      if (sp.mode == kLanes) {
+        writer = e < 64; nent = 4; stride = 64; r_w = e; qt_w = sp.qt[0];
+      } else if (sp.mode == kStreams) {
+        writer = e < 128; nent = 2; stride = 128; r_w = e; qt_w = sp.qt[0];
+      }
+      const int latent_w = qt_w * kTile + r_w;
+      if (writer && latent_w < p.M) {
+        float lmax = -INFINITY;
+        for (int i = 0; i < nent; ++i) lmax = fmaxf(lmax, scr_l[e + i * stride]);
+        float u[D], dsum = 0.f;
+#pragma unroll
+        for (int d = 0; d < D; ++d) u[d] = 0.f;
+        for (int i = 0; i < nent; ++i) {
+          const float li = scr_l[e + i * stride];
+          const float w = li == -INFINITY ? 0.f : __expf(li - lmax);
+          dsum += w;
+#pragma unroll
+          for (int d = 0; d < D; ++d) u[d] = fmaf(w, scr_z[(e + i * stride) * kZs + d], u[d]);
+        }
+        const float invd = dsum > 0.f ? 1.f / dsum : 0.f;
+#pragma unroll
+        for (int d = 0; d < D; ++d) u[d] *= invd;
+        const size_t prow = (((size_t)bh * p.qtiles + qt_w) * p.splits + split) * kTile + r_w;
+        store_row<D>(p.part_z + prow * D, u);
+        p.part_l[prow] = dsum > 0.f ? lmax + __logf(dsum) : -INFINITY;
+      }
     }
     __threadfence();
     softmax_groups_sync();
@@ -516,44 +566,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (sh.last) {
       __threadfence();
       if (threadIdx.x == 128) p.counters[grp] = 0u;  // ready for the next call
-      // each latent row of the group is merged once: by slot 0, and by slot 1
-      // for the second block of a pair
-      const bool merges = valid && (k == 0 || sp.mode == kPair) && (sp.mode != kLanes || row < 64);
-      if (merges) {
-        // Appendix B.3: L_max, d_s = exp(L_s - L_max), U = sum d_s Z_s, Z = U / d
-        float lmax = -INFINITY;
-        for (int s = 0; s < p.splits; ++s)
-          for (int q = 0; q < nstreams; ++q)
-            lmax = fmaxf(lmax, __ldcg(p.part_l + ((blk * p.splits + s) * p.pstreams + q) * kTile + r_in));
-        float u[D], dsum = 0.f;
+      // 3) the last CTA of the group merges the splits (Appendix B.3:
+      //    L_max, d_s = exp(L_s - L_max), U = sum d_s Z_s, Z = U / d), with
+      //    `tpr` threads per latent row sharing the splits
+      const int rows = sp.mode == kLanes ? 64 : (sp.mode == kStreams ? 128 : 256);
+      const int tpr = 256 / rows;
+      const int rg = e / tpr, part = e % tpr;
+      const int qt_f = sp.mode == kPair ? sp.qt[rg >> 7] : sp.qt[0];
+      const int r_f = rg & 127;
+      const int latent_f = qt_f * kTile + r_f;
+      const size_t base = ((size_t)bh * p.qtiles + qt_f) * p.splits * kTile + r_f;
+      float lmax = -INFINITY;
+#pragma unroll 4
+      for (int sidx = part; sidx < p.splits; sidx += tpr)
+        lmax = fmaxf(lmax, __ldcg(p.part_l + base + (size_t)sidx * kTile));
+      float u[D], dsum = 0.f;
 #pragma unroll
-        for (int d = 0; d < D; ++d) u[d] = 0.f;
-        for (int s = 0; s < p.splits; ++s) {
-          for (int q = 0; q < nstreams; ++q) {
-            const size_t r = ((blk * p.splits + s) * p.pstreams + q) * kTile + r_in;
-            const float ls = __ldcg(p.part_l + r);
-            if (ls == -INFINITY) continue;
-            const float w = __expf(ls - lmax);
-            dsum += w;
-            const float4* zr = reinterpret_cast<const float4*>(p.part_z + r * D);
+      for (int d = 0; d < D; ++d) u[d] = 0.f;
+#pragma unroll 2
+      for (int sidx = part; sidx < p.splits; sidx += tpr) {
+        const size_t r = base + (size_t)sidx * kTile;
+        const float ls = __ldcg(p.part_l + r);
+        const float w = ls == -INFINITY ? 0.f : __expf(ls - lmax);
+        dsum += w;
+        const float4* zr = reinterpret_cast<const float4*>(p.part_z + r * D);
 #pragma unroll
-            for (int d = 0; d < D; d += 4) {
-              const float4 zz = __ldcg(zr + d / 4);
-              u[d] = fmaf(w, zz.x, u[d]);
-              u[d + 1] = fmaf(w, zz.y, u[d + 1]);
-              u[d + 2] = fmaf(w, zz.z, u[d + 2]);
-              u[d + 3] = fmaf(w, zz.w, u[d + 3]);
-            }
-          }
+        for (int d = 0; d < D; d += 4) {
+          const float4 zz = __ldcg(zr + d / 4);
+          u[d] = fmaf(w, zz.x, u[d]);
+          u[d + 1] = fmaf(w, zz.y, u[d + 1]);
+          u[d + 2] = fmaf(w, zz.z, u[d + 2]);
+          u[d + 3] = fmaf(w, zz.w, u[d + 3]);
         }
+      }
+      // combine the tpr threads of a row (consecutive lanes of one warp)
+      float gmax = lmax;
+      for (int off = 1; off < tpr; off <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, off));
+      const float sc = lmax == -INFINITY ? 0.f : __expf(lmax - gmax);
+      dsum *= sc;
+#pragma unroll
+      for (int d = 0; d < D; ++d) u[d] *= sc;
+      for (int off = 1; off < tpr; off <<= 1) {
+        dsum += __shfl_xor_sync(0xFFFFFFFFu, dsum, off);
+#pragma unroll
+        for (int d = 0; d < D; ++d) u[d] += __shfl_xor_sync(0xFFFFFFFFu, u[d], off);
+      }
+      if (part == 0 && latent_f < p.M) {
         const float invd = 1.f / dsum;
 #pragma unroll
         for (int d = 0; d < D; ++d) u[d] *= invd;
-        const size_t orow = (size_t)bh * p.M + latent;
+        const size_t orow = (size_t)bh * p.M + latent_f;
         if (kSynth) {
           // gate (eq. 7): Q = N0(Qf) + g * Qd in fp32, cast to bf16
           float f[D];
-          load_row<D>(p.qf + ((size_t)h * p.M + latent) * D, f);
+          load_row<D>(p.qf + ((size_t)h * p.M + latent_f) * D, f);
           float ss = 0.f;
 #pragma unroll
           for (int d = 0; d < D; ++d) ss = fmaf(f[d], f[d], ss);
@@ -576,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int d = 0; d < D; ++d) u[d] = round_as<__nv_bfloat16>(u[d]);
             store_row<D>(p.dbg_a + orow * D, u);
           }
-          if (p.dbg_b) p.dbg_b[orow] = lmax + __logf(dsum);
+          if (p.dbg_b) p.dbg_b[orow] = gmax + __logf(dsum);
         }
       }
     }
@@ -695,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int width = min(kTile, p.M - ch * kTile);
         const uint32_t zc = aZ + ch * L::kTileBytes;
         for (int kk = 0; kk < width / 16; ++kk)
-          mma_ts(tmem + k * kSlotCols + kColO, tmem + k * kSlotCols + kk * 8, L::values1(zc, aOnes, kk), idO,
+          mma_ts(tmem + k * kSlotCols + kColO, tmem + k * kSlotCols + kColP + kk * 8, L::values1(zc, aOnes, kk), idO,
                  (ch > 0 || kk > 0));
         if (ch == chunks - 1) mma_commit(&sh.o_full[k]);
       };
@@ -729,9 +795,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (ch == 0) m = -INFINITY;
       const int width = min(kTile, p.M - ch * kTile);
-      if (width > 64) softmax_step<D, kTile>(tS, tO, width, c, m, ch > 0);
-      else if (width > 32) softmax_step<D, 64>(tS, tO, width, c, m, ch > 0);
-      else softmax_step<D, 32>(tS, tO, width, c, m, ch > 0);
+      if (width > 64) softmax_step<D, kTile>(tS, tS + kColP, tO, width, c, m, ch > 0);
+      else if (width > 32) softmax_step<D, 64>(tS, tS + kColP, tO, width, c, m, ch > 0);
+      else softmax_step<D, 32>(tS, tS + kColP, tO, width, c, m, ch > 0);
       tc_fence_before();
       mbar_arrive(&sh.p_full[k]);
       if (ch == chunks - 1) {
@@ -821,7 +887,7 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
   const dim3 grid(pl.splits, pl.qgroups, BH);
   SplitParams sp{};
   sp.N = pr.N; sp.M = pr.M; sp.H = pr.H;
-  sp.qtiles = pl.tiles; sp.splits = pl.splits; sp.split_len = pl.split_len; sp.pstreams = pl.streams;
+  sp.qtiles = pl.tiles; sp.splits = pl.splits; sp.split_len = pl.split_len;
   sp.part_z = ws.part_z; sp.part_l = ws.part_l;
 
   if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) { *failed = "cudaEventRecord"; return e; }
@@ -880,22 +946,23 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
   return cudaSuccess;
 }
 
-// The split count (per latent group) that fills the SMs best with one CTA
-// per SM: highest fraction of busy SM-waves, fewer splits unless the gain is
-// over 2%, each split at least `min_tiles` token tiles long.
-int choose_splits(long long groups, int n_tiles, int sms, int min_tiles, int forced) {
+// The split count (per latent group) with the least estimated time when each
+// CTA holds one SM: waves x (per-CTA overhead + token tiles per CTA), the
+// overhead counted in token tiles (set-up, pipeline fill, partial results and
+// merge). Fewer splits win ties.
+int choose_splits(long long groups, int n_tiles, int sms, int min_tiles, int overhead_tiles, int forced) {
   if (forced > 0) return std::min(forced, std::max(1, n_tiles));
   const int max_splits = std::max(1, n_tiles / std::max(1, min_tiles));
   int best = 1;
-  double best_eff = -1.0;
-  for (int s = 1; s <= std::min(max_splits, 1024); ++s) {
-    const long long units = groups * s;
-    const long long waves = (units + sms - 1) / sms;
-    if (waves > 8) break;
-    const double eff = (double)units / (double)(waves * sms);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = s;
+  double best_cost = 1e300;
+  for (int s = 1; s <= std::min(max_splits, 2048); ++s) {
+    const int per = (n_tiles + s - 1) / s;
+    const int real = (n_tiles + per - 1) / per;
+    const long long waves = (groups * real + sms - 1) / sms;
+    const double cost = (double)waves * (overhead_tiles + per);
+    if (cost < best_cost * 0.99) {
+      best_cost = cost;
+      best = real;
     }
   }
   return best;
@@ -910,14 +977,14 @@ TcPlan tc_plan(int B, int H, int N, int M, int D, int sms, int forced_splits) {
   const int n_tiles = (N + tc::kTile - 1) / tc::kTile;
   pl.tiles = M <= 64 ? 1 : (M + tc::kTile - 1) / tc::kTile;
   pl.qgroups = M <= 128 ? 1 : (pl.tiles + 1) / 2;
-  pl.streams = M <= 64 ? 4 : ((M <= 128 || pl.tiles % 2 == 1) ? 2 : 1);
+  pl.streams = 1;  // the token streams of a CTA are merged before its partial is written
   // token tiles per split: at least 4 (two per slot) when the sequence allows
-  const int splits = tc::choose_splits(BH * pl.qgroups, n_tiles, std::max(1, sms), 4, forced_splits);
+  const int splits = tc::choose_splits(BH * pl.qgroups, n_tiles, std::max(1, sms), 4, 8, forced_splits);
   const int tiles_per_split = (n_tiles + splits - 1) / splits;
   pl.split_len = tiles_per_split * tc::kTile;
   pl.splits = (N + pl.split_len - 1) / pl.split_len;
   // decode: one CTA per SM over consecutive token tiles of one head
-  const int dsplit = tc::choose_splits(BH, n_tiles, std::max(1, sms), 2, 0);
+  const int dsplit = tc::choose_splits(BH, n_tiles, std::max(1, sms), 2, 4, 0);
   const int per = (n_tiles + dsplit - 1) / dsplit;
   pl.decode_tiles_per_cta = per;
   pl.decode_ctas_per_head = (n_tiles + per - 1) / per;
