@@ -179,6 +179,39 @@ def roofline(costs, stage_ms, peaks, peak_kind, clock_mhz):
             "tensor_frac": round(c["flops"] / t / tensor, 4)}
 
 
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of per-rank timings (the slowest rank counts)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/roofline_traffic.md), or None when it was measured on a
+    different revision of the tensor-core kernels (source hash mismatch)."""
+    import hashlib
+    src = os.path.join(ROOT, "rank_latent_routing_gb300", "csrc", "tc.cu")
+    prof = os.path.join(ROOT, "profiles", "roofline_traffic.md")
+    if not (os.path.exists(src) and os.path.exists(prof)):
+        return None
+    with open(src, "rb") as f:
+        sha = hashlib.sha1(f.read()).hexdigest()[:12]
+    with open(prof) as f:
+        for line in f:
+            if not line.startswith("traffic:"):
+                continue
+            fields = dict(kv.split("=", 1) for kv in line[len("traffic:"):].split())
+            if (fields.get("workload") == workload and fields.get("kernel") == kernel
+                    and fields.get("source_sha1") == sha):
+                return int(fields["bytes_per_launch"])
+    return None
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -265,12 +298,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
-    t_max = total_ms
-    e2e_max = e2e_ms
-    if world > 1:
-        tt = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max, e2e_max = float(tt[0]), float(tt[1])
+    t_max, e2e_max = max_over_ranks([total_ms, e2e_ms], world, device)
     if rank != 0:
         return None
 
@@ -299,6 +327,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": 3 * args.steps,
         "impl": "ours",
     }
+    rl = line["roofline"]
+    rl["traffic"] = measured_traffic(args.workload, rl["kernel"])
     return line
 
 
