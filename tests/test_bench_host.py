@@ -1,0 +1,69 @@
+"""Host-side logic of bench.py without a GPU: the max-over-ranks timing
+reduction on two gloo ranks, the JSON line of the CPU reference arm, and the
+traffic record lookup."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _rank_main(rank, world, port, out_path):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks([10.0 * (rank + 1), 5.0 - rank], world, torch.device("cpu"))
+        if rank == 0:
+            with open(out_path, "w") as f:
+                json.dump(got, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks(tmp_path):
+    import socket
+
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    out = tmp_path / "max.json"
+    mp.spawn(_rank_main, args=(2, port, str(out)), nprocs=2, join=True)
+    assert json.loads(out.read_text()) == [20.0, 5.0]
+
+
+def test_max_over_ranks_single_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks([1.5, 2.5], 1, None) == [1.5, 2.5]
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_record_follows_kernel_source():
+    sys.path.insert(0, ROOT)
+    import bench
+    t = bench.measured_traffic("pde2d", "synthesis")
+    # the committed record matches the committed kernel source
+    assert t is not None and t > 16_000_000
+    assert bench.measured_traffic("pde2d", "no-such-kernel") is None
