@@ -5,26 +5,49 @@
 // Section 3.2 eq. 6 and eq. 8):
 //
 //  * split_kernel — latent queries attend over one token range (split) of a
-//    head. Scores S = Q K^T land in TMEM; one thread per latent row runs an
-//    online softmax over the tokens; P goes back to TMEM in bf16 over the
-//    scores and the tensor core accumulates O += P [V | 1] in TMEM, the
-//    appended ones column giving the softmax row sum. Each split's (Z_s, L_s)
-//    goes to global memory and the last CTA of a head to arrive merges all
-//    splits with the stable log-sum-exp schedule of Appendix B.3 (eq. 29-33).
-//    The synthesis instance normalises each staged Ks_raw tile in place (N0,
-//    eq. 5), uses it as both keys and values (eq. 19) and ends with the gate
-//    (eq. 7): Q = N0(Qf) + g * Qd in fp32, cast to bf16. The encode instance
-//    ends with Z (bf16) and L.
+//    head. Scores S = Q K^T land in TMEM; threads run an online softmax over
+//    the tokens; P goes back to TMEM in bf16 over the scores and the tensor
+//    core accumulates O += P [V | 1] in TMEM, the appended ones column giving
+//    the softmax row sum. Each split's (Z_s, L_s) goes to global memory and
+//    the last CTA of a head to arrive merges all splits with the stable
+//    log-sum-exp schedule of Appendix B.3 (eq. 29-33). The synthesis instance
+//    normalises each staged Ks_raw tile in place (N0, eq. 5), uses it as both
+//    keys and values (eq. 19) and ends with the gate (eq. 7):
+//    Q = N0(Qf) + g * Qd in fp32, cast to bf16. The encode instance ends with
+//    Z (bf16) and L.
 //  * decode_kernel — tokens attend over the M routes: Q and Z of the head stay
 //    in shared memory for all of the CTA's token tiles; S = K Q^T is computed
 //    128 routes at a time with an online softmax over M per token, and
 //    O += P [Z | 1]; out = O / rowsum in bf16.
 //
-// One CTA per SM, 384 threads: warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues the MMAs (one thread), warps 2-3 normalise synthesis tiles, and two
-// softmax warpgroups (warps 4-7 and 8-11) each own one of two TMEM slots, so
-// one slot's softmax runs while the tensor core works on the other's products.
-// Warp w reads TMEM lanes 32*(w%4) .. +31.
+// One CTA per SM, 512 threads: warp 0 issues TMA loads, warps 1-4 issue the
+// MMAs (one thread each, one per (slot, column half); warp 1 owns TMEM),
+// warps 0, 5, 14 and 15 (one per SM sub-partition) normalise a quarter of
+// every synthesis tile each, and two softmax warpgroups (warps 6-9 and
+// 10-13) take the first and the second 64 score columns of every step.
+// Both work on two TMEM slots in turn, so the tensor core computes one slot's
+// products and next scores while the softmax runs on the other. Each (slot,
+// half) is a pipeline of its own: its issuing thread adds the half's products
+// and then writes the half's next 64 score columns, and its warpgroup waits
+// for those alone. A thread spends ~50-80 cycles issuing one tcgen05.mma, so
+// four issuers keep the tensor pipe fed where one or two would not. Warp w
+// reads TMEM lanes 32*(w%4) .. +31.
+//
+// A slot holds 128 score columns and two accumulators, one per column half:
+// each half writes its P in bf16 over the first 32 of its own score columns,
+// and its products go to its own accumulator, so the two halves of a row are
+// two independent softmax streams (own reference, own accumulator) that meet
+// only at the end, in the same log-sum-exp merge as the splits. The next
+// scores are issued after the products that read P; the tensor core runs a
+// thread's MMAs in order.
+//
+// The softmax is one pass: p = 2^(s*c - r) against a reference r (an integer
+// in exp2 units) fixed before the tile; the first tile of a stream sets r
+// from its own max. Whether some p reached 2 is read off the packed bf16
+// results (exponent field >= 128 <=> p >= 2, which also catches inf); only
+// then does the warp read its scores again, move r to 16 units above the
+// ceiling of their max and redo them, and the accumulator is rescaled
+// exactly by 2^(r_old - r_new) before the tile's products are added.
 //
 // Every wait on an mbarrier is bounded: after about a second without progress
 // the thread records kErrTimeout in the device error word, raises the CTA's
@@ -47,13 +70,16 @@ using namespace sm100;
 
 __device__ unsigned g_tc_error = 0u;
 
-constexpr int kThreads = 384;
-constexpr int kTile = 128;          // tokens per staged tile; latents per row block
-constexpr int kStages = 6;          // token-tile ring depth
+constexpr int kThreads = 512;
+constexpr int kWarpIssue = 1;        // first MMA-issuing warp: warp 1 + 2k + hf
+constexpr int kWarpNorm = 5;         // N0 of the synthesis tiles: warps 0, 5, 14 and 15
+constexpr int kWarpSoftmax = 6;      // first softmax warp (6-13)
+constexpr int kTile = 128;           // tokens per staged tile; latents per row block
+constexpr int kMaxStages = 16;       // token-tile ring depth (upper bound)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSlotCols = 256;  // slot s: scores at s*256, accumulator at +128, probabilities at +176
-constexpr uint32_t kColO = 128;
-constexpr uint32_t kColP = 176;
+constexpr uint32_t kSlotCols = 256;  // slot s starts at column 256*s
+constexpr uint32_t kColO = 128;      // accumulator of column half 0; half 1's follows it
+constexpr uint32_t kColQ = 224;      // the slot's latent queries (bf16 pairs), A operand of the scores
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
 
 // How the two TMEM slots of a split-kernel CTA divide the work:
@@ -64,14 +90,15 @@ constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
 enum : int { kLanes = 0, kStreams = 1, kPair = 2 };
 
 struct Shared {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t norm[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t norm[kMaxStages];
   uint64_t q_full;
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_full[2];
-  uint64_t drain;
+  uint64_t s_full[2][2];  // scores of half h of slot k ready (and the half's earlier products done)
+  uint64_t p_full[2][2];  // P of column half h of slot k written
+  uint64_t o_full[2][2];  // the last products of half h of slot k done
+  uint64_t q_tmem;        // the latent queries are in TMEM
+  uint64_t drain;         // every MMA of the CTA has completed
   uint32_t tmem_base;
   int abort;
   int last;
@@ -85,8 +112,21 @@ __device__ __forceinline__ bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_
   return false;
 }
 
+// One arrival per warp: the lanes' TMEM accesses are ordered before the
+// warp's sync, then lane 0 arrives.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Barrier over the two softmax warpgroups only (256 threads).
 __device__ __forceinline__ void softmax_groups_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// 2^e for an integer e <= 0 held in a float (exact; 0 below the normal range).
+__device__ __forceinline__ float pow2_neg(float e) {
+  return e < -126.f ? 0.f : __int_as_float((127 + static_cast<int>(e)) << 23);
+}
 
 template <int D>
 struct Layout {
@@ -125,97 +165,162 @@ __device__ void fill_ones(unsigned char* tile, int tid, int nthreads) {
   }
 }
 
-// Scales the accumulator columns (values and row sum) of this lane by `alpha`.
+// Scales this lane's accumulator (values and row sum) by `alpha`.
 template <int D>
-__device__ __forceinline__ void rescale_acc(uint32_t taddr, float alpha) {
+__device__ __forceinline__ void rescale_acc(uint32_t tO, float alpha) {
   uint32_t r[16];
 #pragma unroll
   for (int c = 0; c < Layout<D>::kNo; c += 16) {
-    tmem_ld16(taddr + c, r);
-    tmem_wait_ld();
+    tmem_ld16(tO + c, r);
+    tmem_wait_ld_regs(r);
 #pragma unroll
     for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-    tmem_st16(taddr + c, r);
+    tmem_st16(tO + c, r);
   }
   tmem_wait_st();
 }
 
 // Reads the D output values and the row sum of this lane's accumulator.
 template <int D>
-__device__ __forceinline__ float load_acc(uint32_t taddr, float (&o)[D]) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
+__device__ __forceinline__ float load_acc(uint32_t tO, float (&o)[D]) {
+  uint32_t a[32];
+  tmem_ld32(tO, a);
   if (D == 32) {
     uint32_t s[16];
-    tmem_ld16(taddr + 32, s);
-    tmem_wait_ld();
+    tmem_ld16(tO + 32, s);
+    tmem_wait_ld_regs(a);
+    tmem_wait_ld_regs(s);
 #pragma unroll
-    for (int i = 0; i < D; ++i) o[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < D; ++i) o[i] = __uint_as_float(a[i]);
     return __uint_as_float(s[0]);
   }
-  tmem_wait_ld();
+  tmem_wait_ld_regs(a);
 #pragma unroll
-  for (int i = 0; i < D; ++i) o[i] = __uint_as_float(r[i]);
-  return __uint_as_float(r[D]);
+  for (int i = 0; i < D; ++i) o[i] = __uint_as_float(a[i]);
+  return __uint_as_float(a[D]);
 }
 
-// One softmax step over `kWidth` (32, 64 or 128) score columns of this lane,
-// columns >= `valid` masked. `m` is the running max in raw score units; it
-// moves only when the tile max exceeds it by more than 2^8 in exp2 units
-// (then the accumulator, row sum included, is rescaled), so p <= 256. P is
-// written in bf16 to the kWidth/2 probability columns at tP. The scores are
-// read twice (max, then exponentials), 64 columns at a time, to keep the
-// live registers low. Warp-uniform: every lane of a warp calls it with the
-// same width and valid count.
-template <int D, int kWidth>
-__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tP, uint32_t tO, int valid, float c,
-                                             float& m, bool has_acc) {
-  constexpr float kLazy = 8.0f;
-  constexpr int kPart = kWidth < 64 ? kWidth : 64;
-  float tmax = m;
+// ------------------------------------------------------------- softmax step
+// Reads this lane's 64 scores of a column half and masks the columns at or
+// past `valid` (1..64).
+__device__ __forceinline__ void load_half(uint32_t tS, int valid, uint32_t (&s)[64]) {
+  tmem_ld64(tS, s);
+  tmem_wait_ld_regs(s);
+  if (valid < 64) {
 #pragma unroll
-  for (int base = 0; base < kWidth; base += kPart) {
-    uint32_t r[kPart];
-#pragma unroll
-    for (int b = 0; b < kPart; b += 32) tmem_ld32(tS + base + b, *reinterpret_cast<uint32_t(*)[32]>(r + b));
-    tmem_wait_ld();
-    if (valid < base + kPart) {
-#pragma unroll
-      for (int i = 0; i < kPart; ++i)
-        if (base + i >= valid) r[i] = __float_as_uint(-INFINITY);
-    }
-#pragma unroll
-    for (int i = 0; i < kPart; i += 2) tmax = max3(tmax, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+    for (int i = 0; i < 64; ++i)
+      if (i >= valid) s[i] = __float_as_uint(-INFINITY);
   }
-  const bool grow = tmax > m && (m == -INFINITY || (tmax - m) * c > kLazy);
-  float alpha = 1.f;
-  if (grow) {
-    alpha = m == -INFINITY ? 0.f : ex2((m - tmax) * c);
-    m = tmax;
-  }
-  if (has_acc && __any_sync(0xFFFFFFFFu, grow)) rescale_acc<D>(tO, alpha);
+}
+
+// p = 2^(s*c - r) of the 64 columns, packed in bf16 pairs into s[0..31];
+// returns the OR of the packed words.
+__device__ __forceinline__ uint32_t exp_pack(uint32_t (&s)[64], float c, float r) {
   const float2 cc = make_float2(c, c);
-  const float2 mc = make_float2(-m * c, -m * c);
+  const float2 rr = make_float2(-r, -r);
+  uint32_t o0 = 0u, o1 = 0u;
 #pragma unroll
-  for (int base = 0; base < kWidth; base += kPart) {
-    uint32_t r[kPart];
-#pragma unroll
-    for (int b = 0; b < kPart; b += 32) tmem_ld32(tS + base + b, *reinterpret_cast<uint32_t(*)[32]>(r + b));
-    tmem_wait_ld();
-    if (valid < base + kPart) {
-#pragma unroll
-      for (int i = 0; i < kPart; ++i)
-        if (base + i >= valid) r[i] = __float_as_uint(-INFINITY);
-    }
-#pragma unroll
-    for (int i = 0; i < kPart / 2; ++i) {
-      const float2 x = fma2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), cc, mc);
-      r[i] = pack_bf16x2(ex2(x.x), ex2(x.y));
-    }
-    if (kPart == 64) tmem_st32(tP + base / 2, *reinterpret_cast<uint32_t(*)[32]>(r));
-    else tmem_st16(tP + base / 2, *reinterpret_cast<uint32_t(*)[16]>(r));
+  for (int i = 0; i < 32; ++i) {
+    const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), cc, rr);
+    s[i] = pack_bf16x2(ex2(x.x), ex2(x.y));
+    if (i & 1) o1 |= s[i];
+    else o0 |= s[i];
   }
+  return o0 | o1;
+}
+
+// Exponent field >= 128 in either bf16 half: some p >= 2 (or inf / NaN).
+constexpr uint32_t kGrowBits = 0x40004000u;
+// When the reference moves it is set this many exp2 units above the tile max,
+// so that p <= 2^-16 and the next move waits for the max to grow by 17 units
+// (p that small loses nothing: fp32 and bf16 keep their relative precision
+// down to 2^-126).
+constexpr float kHeadroom = 16.0f;
+
+__device__ __forceinline__ float half_max(const uint32_t (&s)[64]) {
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 64; i += 4) {
+    m0 = max3(m0, __uint_as_float(s[i]), __uint_as_float(s[i + 1]));
+    m1 = max3(m1, __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
+  }
+  return fmaxf(m0, m1);
+}
+
+// One softmax step of this lane over its column half at tS: `valid` (<= 64)
+// columns, P (32 packed columns) written over the first 32. The first tile
+// of a stream (r = -inf, the same for the whole warp) takes its reference
+// from its own max; later tiles are done against r in one pass, and only if
+// some p reached 2 is the half read again and redone against a new r.
+// Warp-uniform `valid`.
+__device__ __forceinline__ void softmax_half(uint32_t tS, int valid, float c, float& r) {
+  uint32_t s[64];
+  load_half(tS, valid, s);
+  if (__any_sync(0xFFFFFFFFu, r == -INFINITY)) {
+    const float m = half_max(s);
+    if (r == -INFINITY) r = ceilf(m * c) + kHeadroom;
+    exp_pack(s, c, r);
+  } else {
+    const uint32_t bits = exp_pack(s, c, r);
+    if (__any_sync(0xFFFFFFFFu, (bits & kGrowBits) != 0u)) {
+      // the scores are still in TMEM
+      load_half(tS, valid, s);
+      const float m = half_max(s);
+      if ((bits & kGrowBits) != 0u) r = ceilf(m * c) + kHeadroom;
+      exp_pack(s, c, r);
+    }
+  }
+  tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(s));
+}
+
+// End of a softmax step: the products of the previous step are in (this
+// step's scores were issued after them), so the accumulator is brought to the
+// reference of the probabilities just written; then P goes to the tensor core.
+template <int D>
+__device__ __forceinline__ void finish_half(uint64_t* p_full, uint32_t tO, float r, float& ro, bool acc) {
   tmem_wait_st();
+  const bool need = acc && ro != r;
+  if (__any_sync(0xFFFFFFFFu, need)) rescale_acc<D>(tO, need ? pow2_neg(ro - r) : 1.f);
+  ro = r;
+  warp_arrive(p_full);
+}
+
+// N0 (eq. 5) of rows 32*part + lane of staged synthesis tile t, in place, in
+// the swizzled layout (a row's 16-byte chunks are permuted within the row,
+// which the sum of squares and the scaling do not see); one arrival per warp
+// on the tile's barrier. Returns false if the wait for the tile gave up.
+template <int D, int kStages>
+__device__ __forceinline__ bool normalise_part(Shared& sh, unsigned char* sStage, uint32_t stage_bytes, int t,
+                                               int part, int lane) {
+  using L = Layout<D>;
+  const int s = t % kStages;
+  if (!wait_or_abort(sh, &sh.full[s], (t / kStages) & 1)) return false;
+  uint4* row = reinterpret_cast<uint4*>(sStage + s * stage_bytes + (32 * part + lane) * L::kRowBytes);
+  uint4 v[D / 8];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) {
+    v[i] = row[i];
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float a = __uint_as_float(w[q] << 16), b = __uint_as_float(w[q] & 0xFFFF0000u);
+      ss = fmaf(a, a, fmaf(b, b, ss));
+    }
+  }
+  const float r = rsqrtf(ss / (float)D + kEps);
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) {
+    uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = pack_bf16x2(__uint_as_float(w[q] << 16) * r, __uint_as_float(w[q] & 0xFFFF0000u) * r);
+    row[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sh.norm[s]);
+  return true;
 }
 
 // ------------------------------------------------------------ split kernel
@@ -265,16 +370,33 @@ __device__ __forceinline__ int slot_tile(const SlotPlan& s, int k, int j) {
   return j;
 }
 
+// Epilogue scratch of the split kernel: (L, Z) of 512 softmax streams.
+template <int D>
+__host__ __device__ constexpr int split_scratch_bytes() {
+  return 512 * 4 + 512 * (D + 1) * 4;
+}
+
+// Token-tile ring depth of the split kernel: as deep as fits next to the
+// latent tiles and the ones tile (within ~200 KB).
+template <int D, bool kSynth>
+__host__ __device__ constexpr int split_stages() {
+  constexpr int stage = (kSynth ? 1 : 2) * Layout<D>::kTileBytes;
+  constexpr int n = (200 * 1024 - 3 * Layout<D>::kTileBytes) / stage;
+  return n > kMaxStages ? kMaxStages : n;
+}
+
 template <int D, bool kSynth>
 __global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
   using L = Layout<D>;
+  constexpr int kStages = split_stages<D, kSynth>();
+  constexpr uint32_t kStageBytes = kSynth ? L::kTileBytes : 2 * L::kTileBytes;
+  static_assert(kStages * (int)kStageBytes >= split_scratch_bytes<D>(), "epilogue scratch exceeds the stage ring");
   extern __shared__ unsigned char smem_raw[];
   __shared__ Shared sh;
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-  constexpr uint32_t kStageBytes = kSynth ? L::kTileBytes : 2 * L::kTileBytes;
   unsigned char* sQ = smem;                                   // [2][128][D]
   unsigned char* sStage = smem + 2 * L::kTileBytes;           // [kStages] x (K, V)
   unsigned char* sOnes = sStage + kStages * kStageBytes;      // [128][D] rows [1, 0, ...]
@@ -287,20 +409,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_end = min(p.N, n_begin + p.split_len);
   const int T = n_begin < n_end ? (n_end - n_begin + kTile - 1) / kTile : 0;
   const SlotPlan sp = slot_plan(p.M, p.qtiles, group, T);
+  const int jmax = max(sp.steps[0], sp.steps[1]);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], 1);
-      mbar_init(&sh.norm[s], 64);
+      mbar_init(&sh.empty[s], sp.mode == kPair ? 4 : 2);  // one release per issuing thread that reads the tile
+      mbar_init(&sh.norm[s], 4);                          // one arrival per normaliser warp
     }
     mbar_init(&sh.q_full, 1);
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(&sh.s_full[k], 1);
-      mbar_init(&sh.p_full[k], 128);
-      mbar_init(&sh.o_full[k], 1);
-    }
-    mbar_init(&sh.drain, 1);
+    for (int k = 0; k < 2; ++k)
+      for (int hf = 0; hf < 2; ++hf) {
+        mbar_init(&sh.s_full[k][hf], 1);
+        mbar_init(&sh.p_full[k][hf], 4);  // one arrival per softmax warp of the half
+        mbar_init(&sh.o_full[k][hf], 1);
+      }
+    mbar_init(&sh.drain, 4);
+    mbar_init(&sh.q_tmem, 4);
     sh.abort = 0;
     sh.last = 0;
     fence_mbar_init();
@@ -309,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&sh.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 4) fill_ones<D>(sOnes, threadIdx.x - 128, 256);
+  if (warp >= kWarpSoftmax && warp < kWarpSoftmax + 8) fill_ones<D>(sOnes, threadIdx.x - 32 * kWarpSoftmax, 256);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -318,6 +443,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // (in the synthesis instance the warp also normalises rows 0-31 of each
+    // tile, kStages / 2 tiles behind the loads its lane 0 issues: the load of
+    // tile t waits for tile t - kStages to be released, which in the lanes
+    // mode needs tile t - kStages + 1 normalised, so the lag must stay below
+    // kStages - 1)
+    constexpr int kLag = kSynth ? kStages / 2 : 0;
+    static_assert(kLag <= kStages - 2, "normaliser lag would deadlock the ring");
+    int issued = 0;
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
@@ -332,40 +465,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sQ, &tm_q, &sh.q_full, 0, sp.qt[0] * kTile, qz);
         if (sp.mode == kPair) tma_load_3d(sQ + L::kTileBytes, &tm_q, &sh.q_full, 0, sp.qt[1] * kTile, qz);
       }
-      int issued = 0;
-      for (int t = 0; t < T; ++t) {
+    }
+    bool ok = true;
+    for (int t = 0; t < T + kLag; ++t) {
+      if (lane == 0 && ok && t < T) {
         const int s = t % kStages;
-        if (t >= kStages && !wait_or_abort(sh, &sh.empty[s], ((t / kStages) - 1) & 1)) break;
-        unsigned char* dst = sStage + s * kStageBytes;
-        mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
-        tma_load_3d(dst, &tm_k, &sh.full[s], 0, n_begin + t * kTile, bh);
-        if (!kSynth) tma_load_3d(dst + L::kTileBytes, &tm_v, &sh.full[s], 0, n_begin + t * kTile, bh);
-        issued = t + 1;
+        if (t >= kStages && !wait_or_abort(sh, &sh.empty[s], ((t / kStages) - 1) & 1)) {
+          ok = false;
+        } else {
+          unsigned char* dst = sStage + s * kStageBytes;
+          mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
+          tma_load_3d(dst, &tm_k, &sh.full[s], 0, n_begin + t * kTile, bh);
+          if (!kSynth) tma_load_3d(dst + L::kTileBytes, &tm_v, &sh.full[s], 0, n_begin + t * kTile, bh);
+          issued = t + 1;
+        }
       }
-      if (*(volatile int*)&sh.abort) {
-        // let the copies still in flight land before the CTA leaves
-        for (int t = max(0, issued - kStages); t < issued; ++t)
-          mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, kWaitLimit);
-        mbar_wait(&sh.q_full, 0, kWaitLimit);
+      if (kSynth) {
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        const int tn = t - kLag;
+        if (ok && tn >= 0) ok = normalise_part<D, kStages>(sh, sStage, kStageBytes, tn, 0, lane);
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA
+    if (lane == 0 && *(volatile int*)&sh.abort) {
+      // let the copies still in flight land before the CTA leaves
+      for (int t = max(0, issued - kStages); t < issued; ++t)
+        mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, kWaitLimit);
+      mbar_wait(&sh.q_full, 0, kWaitLimit);
+    }
+  } else if (warp < kWarpNorm) {
+    // ---------------------------------- MMA of column half hf of slot kk
     if (lane == 0) {
-      const uint32_t aQ0 = smem_u32(sQ);
-      const uint32_t aQ1 = sp.mode == kPair ? aQ0 + L::kTileBytes : aQ0;
+      const int kk = (warp - kWarpIssue) >> 1, hf = (warp - kWarpIssue) & 1;
       const uint32_t aOnes = smem_u32(sOnes);
-      const uint32_t idS = idesc_bf16(128, kTile, false, false);
+      const uint32_t idS = idesc_bf16(128, 64, false, false);
       const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
+      const uint32_t rows_off = hf * 64 * L::kRowBytes;  // first token row of the half in a tile
       constexpr uint32_t kLo = 0u, kAll = 0xFFFFFFFFu;
       auto stage_addr = [&](int t) { return smem_u32(sStage + (t % kStages) * kStageBytes); };
       auto ready = [&](int t) -> bool {
         return wait_or_abort(sh, kSynth ? &sh.norm[t % kStages] : &sh.full[t % kStages], (t / kStages) & 1);
       };
-      // scores of slot k, step j
+      // scores of the half's 64 token columns of slot k, step j; the latent
+      // queries (A) are read from TMEM, the keys (B) from the staged tile
       auto issue_s = [&](int k, int j) -> bool {
-        const uint32_t dS = tmem + k * kSlotCols;
-        const uint32_t aQ = k == 0 ? aQ0 : aQ1;
+        const uint32_t dS = tmem + k * kSlotCols + 64 * hf;
+        const uint32_t tQ = tmem + k * kSlotCols + kColQ;
         const int t = slot_tile(sp, k, j);
         if (!ready(t)) return false;
         if (sp.mode == kLanes) {
@@ -374,178 +518,181 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int q = 0; q < D / 16; ++q)
-            mma_ss_masked(dS, L::kmajor(aQ, q), L::kmajor(stage_addr(t), q), idS, q > 0, kLo, kLo, kAll, kAll);
+            mma_ts_masked(dS, tQ + q * 8, L::kmajor(stage_addr(t) + rows_off, q), idS, q > 0, kLo, kLo, kAll, kAll);
           if (has_b) {
 #pragma unroll
             for (int q = 0; q < D / 16; ++q)
-              mma_ss_masked(dS, L::kmajor(aQ, q), L::kmajor(stage_addr(t + 1), q), idS, q > 0, kAll, kAll, kLo,
+              mma_ts_masked(dS, tQ + q * 8, L::kmajor(stage_addr(t + 1) + rows_off, q), idS, q > 0, kAll, kAll, kLo,
                             kLo);
           }
         } else {
           tc_fence_after();
 #pragma unroll
-          for (int q = 0; q < D / 16; ++q) mma_ss(dS, L::kmajor(aQ, q), L::kmajor(stage_addr(t), q), idS, q > 0);
+          for (int q = 0; q < D / 16; ++q) mma_ts(dS, tQ + q * 8, L::kmajor(stage_addr(t) + rows_off, q), idS, q > 0);
         }
-        mma_commit(&sh.s_full[k]);
+        mma_commit(&sh.s_full[k][hf]);
         return true;
       };
-      // O += P [V | 1] for slot k, step j; releases the tiles no longer needed
+      // O_hf += P_hf [V | 1]_hf for slot k, step j: slices 4hf .. 4hf+3 of the
+      // tile, P of the half at column 64hf of the slot
       auto issue_pv = [&](int k, int j) {
-        const uint32_t dO = tmem + k * kSlotCols + kColO;
-        const uint32_t aP = tmem + k * kSlotCols + kColP;
+        const uint32_t dO = tmem + k * kSlotCols + kColO + hf * L::kNo;
+        const uint32_t aP = tmem + k * kSlotCols + 64 * hf;
         const int t = slot_tile(sp, k, j);
         const uint32_t vA = stage_addr(t) + (kSynth ? 0 : L::kTileBytes);
         if (sp.mode == kLanes) {
           const bool has_b = t + 1 < T;
           const uint32_t vB = stage_addr(t + 1) + (kSynth ? 0 : L::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts_masked(dO, aP + kk * 8, L::values1(vA, aOnes, kk), idO, (j > 0 || kk > 0), kLo, kLo, kAll, kAll);
+          for (int i = 0; i < 4; ++i)
+            mma_ts_masked(dO, aP + i * 8, L::values1(vA, aOnes, 4 * hf + i), idO, (j > 0 || i > 0), kLo, kLo, kAll,
+                          kAll);
           if (has_b) {
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ts_masked(dO, aP + kk * 8, L::values1(vB, aOnes, kk), idO, (j > 0 || kk > 0), kAll, kAll, kLo,
-                            kLo);
+            for (int i = 0; i < 4; ++i)
+              mma_ts_masked(dO, aP + i * 8, L::values1(vB, aOnes, 4 * hf + i), idO, (j > 0 || i > 0), kAll, kAll,
+                            kLo, kLo);
           }
-          mma_commit(&sh.empty[t % kStages]);
-          if (has_b) mma_commit(&sh.empty[(t + 1) % kStages]);
         } else {
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(dO, aP + kk * 8, L::values1(vA, aOnes, kk), idO, (j > 0 || kk > 0));
-          if (sp.mode == kStreams || k == 1) mma_commit(&sh.empty[t % kStages]);
+          for (int i = 0; i < 4; ++i)
+            mma_ts(dO, aP + i * 8, L::values1(vA, aOnes, 4 * hf + i), idO, (j > 0 || i > 0));
         }
       };
-      bool ok = wait_or_abort(sh, &sh.q_full, 0);
-      for (int k = 0; ok && k < 2; ++k)
-        if (sp.steps[k] > 0) ok = issue_s(k, 0);
-      const int jmax = max(sp.steps[0], sp.steps[1]);
-      for (int j = 0; ok && j < jmax; ++j) {
-        for (int k = 0; ok && k < 2; ++k) {
-          if (j >= sp.steps[k]) continue;
-          if (!wait_or_abort(sh, &sh.p_full[k], j & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(k, j);
-          if (j + 1 < sp.steps[k]) ok = issue_s(k, j + 1);
-        }
+      // the stage(s) of the step can be refilled once this thread's products
+      // of them are done (every issuing thread that read them releases)
+      auto release = [&](int k, int j) {
+        const int t = slot_tile(sp, k, j);
+        mma_commit(&sh.empty[t % kStages]);
+        if (sp.mode == kLanes && t + 1 < T) mma_commit(&sh.empty[(t + 1) % kStages]);
+      };
+      bool ok = sp.steps[kk] > 0 && wait_or_abort(sh, &sh.q_tmem, 0);
+      tc_fence_after();
+      if (ok) ok = issue_s(kk, 0);
+      for (int j = 0; ok && j < sp.steps[kk]; ++j) {
+        if (!wait_or_abort(sh, &sh.p_full[kk][hf], j & 1)) break;
+        tc_fence_after();
+        issue_pv(kk, j);
+        release(kk, j);
+        if (j + 1 < sp.steps[kk]) ok = issue_s(kk, j + 1);
       }
-      mma_commit(&sh.o_full[0]);
-      mma_commit(&sh.o_full[1]);
       // every MMA of this CTA completes before TMEM is released
       mma_commit(&sh.drain);
       mbar_wait(&sh.drain, 0, kWaitLimit);
     }
-  } else if (warp < 4) {
+  } else if (warp == kWarpNorm || warp >= kWarpSoftmax + 8) {
     // ------------------------------------------- N0 of the synthesis tiles
     if (kSynth) {
-      const int nt = threadIdx.x - 64;  // 0..63: rows nt and nt + 64 of each tile
-      for (int t = 0; t < T; ++t) {
-        const int s = t % kStages;
-        if (!wait_or_abort(sh, &sh.full[s], (t / kStages) & 1)) break;
-        unsigned char* tileb = sStage + s * kStageBytes;
+      const int part = warp == kWarpNorm ? 1 : warp - (kWarpSoftmax + 6);  // 1, 2, 3
+      for (int t = 0; t < T; ++t)
+        if (!normalise_part<D, kStages>(sh, sStage, kStageBytes, t, part, lane)) break;
+    }
+  } else if (warp >= kWarpSoftmax && warp < kWarpSoftmax + 8) {
+    // ------------------------------------------------- softmax + epilogue
+    const int tid = threadIdx.x - 32 * kWarpSoftmax;  // 0..255
+    const int hf = tid >> 7;                           // column half
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int lanes_half = sp.mode == kLanes ? (row >> 6) : 0;
+    const float c = rsqrtf((float)D) * kLog2e;
+    float r[2] = {-INFINITY, -INFINITY}, ro[2] = {-INFINITY, -INFINITY};  // references of P and of O
+    bool acc[2] = {false, false};
+    bool ok = true;
+    if (hf == 0) {
+      // latent query row `row` of each slot's block from the staged tile into
+      // the slot's Q columns (lane = latent row, bf16 pairs)
+      ok = wait_or_abort(sh, &sh.q_full, 0);
+      if (ok) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint4* row = reinterpret_cast<uint4*>(tileb + (nt + 64 * half) * L::kRowBytes);
-          uint4 v[D / 8];
-          float ss = 0.f;
+        for (int k = 0; k < 2; ++k) {
+          const unsigned char* src = sQ + (sp.mode == kPair ? k * L::kTileBytes : 0);
+          uint32_t w[D / 2];
 #pragma unroll
-          for (int i = 0; i < D / 8; ++i) {
-            v[i] = row[i];
-            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float a = __uint_as_float(w[q] << 16), b = __uint_as_float(w[q] & 0xFFFF0000u);
-              ss = fmaf(a, a, fmaf(b, b, ss));
-            }
+          for (int cc = 0; cc < D / 8; ++cc) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + L::chunk_offset(row, cc));
+            w[4 * cc] = v.x; w[4 * cc + 1] = v.y; w[4 * cc + 2] = v.z; w[4 * cc + 3] = v.w;
           }
-          const float r = rsqrtf(ss / (float)D + kEps);
+          const uint32_t tQ = tmem + lane_base + k * kSlotCols + kColQ;
+          if (D == 32) tmem_st16(tQ, *reinterpret_cast<uint32_t(*)[16]>(w));
+          else tmem_st8(tQ, *reinterpret_cast<uint32_t(*)[8]>(w));
+        }
+        tmem_wait_st();
+      }
+      warp_arrive(&sh.q_tmem);
+    }
+    for (int j = 0; ok && j < jmax; ++j) {
 #pragma unroll
-          for (int i = 0; i < D / 8; ++i) {
-            uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      for (int k = 0; k < 2; ++k) {
+        if (!ok || j >= sp.steps[k]) continue;
+        const uint32_t tS = tmem + lane_base + k * kSlotCols + 64 * hf;
+        const uint32_t tO = tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo;
+        if (!wait_or_abort(sh, &sh.s_full[k][hf], j & 1)) { ok = false; continue; }
+        tc_fence_after();
+        const int t = slot_tile(sp, k, j) + lanes_half;
+        bool wrote = false;
+        if (t < T) {
+          const int valid = min(kTile, n_end - (n_begin + t * kTile)) - 64 * hf;
+          if (valid > 0) {
+            softmax_half(tS, min(valid, 64), c, r[k]);
+            wrote = true;
+          } else {
+            // no token in this half of the last tile: P = 0
+            uint32_t z[32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              w[q] = pack_bf16x2(__uint_as_float(w[q] << 16) * r, __uint_as_float(w[q] & 0xFFFF0000u) * r);
-            row[i] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int i = 0; i < 32; ++i) z[i] = 0u;
+            tmem_st32(tS, z);
           }
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&sh.norm[s]);
+        finish_half<D>(&sh.p_full[k][hf], tO, r[k], ro[k], acc[k]);
+        if (wrote) acc[k] = true;
       }
     }
-  } else {
-    // ------------------------------------------------- softmax + epilogue
-    const int k = (warp - 4) >> 2;  // slot
-    const int row = (threadIdx.x - 128) & 127;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t tS = tmem + lane_base + k * kSlotCols;
-    const uint32_t tO = tS + kColO;
-    const int half = sp.mode == kLanes ? (row >> 6) : 0;
-    const int r_in = sp.mode == kLanes ? (row & 63) : row;
-    const int qt = sp.qt[k];
-    const int latent = qt * kTile + r_in;
-    const bool valid = latent < p.M;
-    const float c = rsqrtf((float)D) * kLog2e;
-    float m = -INFINITY;
-    bool has_acc = false;
-    bool ok = true;
-    for (int j = 0; j < sp.steps[k]; ++j) {
-      if (!wait_or_abort(sh, &sh.s_full[k], j & 1)) { ok = false; break; }
-      tc_fence_after();
-      const int t = slot_tile(sp, k, j) + half;
-      if (t < T) {
-        const int n0 = n_begin + t * kTile;
-        softmax_step<D, kTile>(tS, tS + kColP, tO, min(kTile, n_end - n0), c, m, has_acc);
-        has_acc = true;
-      }
-      tc_fence_before();
-      mbar_arrive(&sh.p_full[k]);
-    }
-    // both slots' products are complete before the stage buffers are reused
-    // as scratch below
-    if (ok) ok = wait_or_abort(sh, &sh.o_full[k], 0);
-    if (ok) ok = wait_or_abort(sh, &sh.o_full[k ^ 1], 0);
+    // every product is complete before the stage buffers are reused as
+    // scratch below
+    if (ok) ok = wait_or_abort(sh, &sh.drain, 0);
     tc_fence_after();
-    float o[D];
-    const float l = load_acc<D>(tO, o);
-    (void)valid;
 
-    // 1) each token stream's (L, Z) into shared memory
+    // 1) each softmax stream's (L, Z) into shared memory: stream e =
+    //    256 hf + 128 k + row
     constexpr int kZs = D + 1;  // padded row stride
-    float* scr_l = reinterpret_cast<float*>(sStage);  // [256]
-    float* scr_z = scr_l + 256;                       // [256][D + 1]
-    const int e = threadIdx.x - 128;
-    {
-      const bool any = ok && has_acc && l > 0.f;  // a stream with no token never wrote its accumulator
+    float* scr_l = reinterpret_cast<float*>(sStage);  // [512]
+    float* scr_z = scr_l + 512;                       // [512][D + 1]
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float o[D];
+      const float l = load_acc<D>(tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo, o);
+      const int e = 256 * hf + 128 * k + row;
+      const bool any = ok && acc[k] && l > 0.f;  // a stream with no token never wrote its accumulator
       const float inv = any ? 1.f / l : 0.f;
-      scr_l[e] = any ? (m * c + __log2f(l)) * kLn2 : -INFINITY;
+      scr_l[e] = any ? (ro[k] + __log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll
       for (int d = 0; d < D; ++d) scr_z[e * kZs + d] = any ? o[d] * inv : 0.f;
     }
     softmax_groups_sync();
 
-    // 2) one partial result per (latent row, split): the CTA's token streams of
-    //    a row merged first (Appendix B.3 schedule over the streams)
+    // 2) one partial result per (latent row, split): the CTA's streams of a
+    //    row merged first (Appendix B.3 schedule over the streams). Stream e
+    //    belongs to latent row (e & 127) of block qt of slot (e >> 7) & 1; in
+    //    the lanes mode row r and r + 64 hold the same latent.
     {
-      int nent = 1, stride = 0, r_w = row, qt_w = sp.qt[k];
-      bool writer = true;
-      if (sp.mode == kLanes) {
-        writer = e < 64; nent = 4; stride = 64; r_w = e; qt_w = sp.qt[0];
-      } else if (sp.mode == kStreams) {
-        writer = e < 128; nent = 2; stride = 128; r_w = e; qt_w = sp.qt[0];
-      }
-      const int latent_w = qt_w * kTile + r_w;
-      if (writer && latent_w < p.M) {
+      const int nwriters = sp.mode == kLanes ? 64 : (sp.mode == kStreams ? 128 : 256);
+      const int nent = 512 / nwriters;
+      for (int e = tid; e < nwriters; e += 256) {
+        const int r_w = e & 127;
+        const int qt_w = sp.mode == kPair ? sp.qt[e >> 7] : sp.qt[0];
+        const int latent_w = qt_w * kTile + r_w;
+        if (latent_w >= p.M) continue;
         float lmax = -INFINITY;
-        for (int i = 0; i < nent; ++i) lmax = fmaxf(lmax, scr_l[e + i * stride]);
+        for (int i = 0; i < nent; ++i) lmax = fmaxf(lmax, scr_l[e + i * nwriters]);
         float u[D], dsum = 0.f;
 #pragma unroll
         for (int d = 0; d < D; ++d) u[d] = 0.f;
         for (int i = 0; i < nent; ++i) {
-          const float li = scr_l[e + i * stride];
+          const float li = scr_l[e + i * nwriters];
           const float w = li == -INFINITY ? 0.f : __expf(li - lmax);
           dsum += w;
 #pragma unroll
-          for (int d = 0; d < D; ++d) u[d] = fmaf(w, scr_z[(e + i * stride) * kZs + d], u[d]);
+          for (int d = 0; d < D; ++d) u[d] = fmaf(w, scr_z[(e + i * nwriters) * kZs + d], u[d]);
         }
         const float invd = dsum > 0.f ? 1.f / dsum : 0.f;
 #pragma unroll
@@ -558,20 +705,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     softmax_groups_sync();
     const size_t grp = (size_t)bh * gridDim.y + group;
-    if (threadIdx.x == 128) {
+    if (tid == 0) {
       const unsigned prev = atomicAdd(p.counters + grp, 1u);
       sh.last = prev == (unsigned)(p.splits - 1);
     }
     softmax_groups_sync();
     if (sh.last) {
       __threadfence();
-      if (threadIdx.x == 128) p.counters[grp] = 0u;  // ready for the next call
+      if (tid == 0) p.counters[grp] = 0u;  // ready for the next call
       // 3) the last CTA of the group merges the splits (Appendix B.3:
       //    L_max, d_s = exp(L_s - L_max), U = sum d_s Z_s, Z = U / d), with
       //    `tpr` threads per latent row sharing the splits
       const int rows = sp.mode == kLanes ? 64 : (sp.mode == kStreams ? 128 : 256);
       const int tpr = 256 / rows;
-      const int rg = e / tpr, part = e % tpr;
+      const int rg = tid / tpr, part = tid % tpr;
       const int qt_f = sp.mode == kPair ? sp.qt[rg >> 7] : sp.qt[0];
       const int r_f = rg & 127;
       const int latent_f = qt_f * kTile + r_f;
@@ -585,11 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int d = 0; d < D; ++d) u[d] = 0.f;
 #pragma unroll 2
       for (int sidx = part; sidx < p.splits; sidx += tpr) {
-        const size_t r = base + (size_t)sidx * kTile;
-        const float ls = __ldcg(p.part_l + r);
+        const size_t rr = base + (size_t)sidx * kTile;
+        const float ls = __ldcg(p.part_l + rr);
         const float w = ls == -INFINITY ? 0.f : __expf(ls - lmax);
         dsum += w;
-        const float4* zr = reinterpret_cast<const float4*>(p.part_z + r * D);
+        const float4* zr = reinterpret_cast<const float4*>(p.part_z + rr * D);
 #pragma unroll
         for (int d = 0; d < D; d += 4) {
           const float4 zz = __ldcg(zr + d / 4);
@@ -655,9 +802,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ----------------------------------------------------------- decode kernel
 struct DecodeParams {
-  int N, M, tiles_per_cta;
+  int N, M, tiles_per_cta, stages;
   __nv_bfloat16* out;  // [BH][N][D]
 };
+
+// Exchange buffer of the decode kernel: the second column half's (L, Z) of
+// each row of both slots, read by the first half to form the output.
+template <int D>
+__host__ __device__ constexpr int decode_xchg_bytes() {
+  return 2 * 128 * (D + 1) * 4;
+}
+
+// Token-tile ring depth of the decode kernel for M routes.
+template <int D>
+__host__ __device__ constexpr int decode_stages(int M) {
+  const int chunks = (M + kTile - 1) / kTile;
+  const int n = (210 * 1024 - decode_xchg_bytes<D>() - (2 * chunks + 1) * (int)Layout<D>::kTileBytes) /
+                (int)Layout<D>::kTileBytes;
+  return n > kMaxStages ? kMaxStages : n;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -669,10 +832,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   const int chunks = (p.M + kTile - 1) / kTile;
+  const int stages = p.stages;
   unsigned char* sQ = smem;                                // [chunks][128][D]
   unsigned char* sZ = smem + chunks * L::kTileBytes;       // [chunks][128][D]
-  unsigned char* sK = smem + 2 * chunks * L::kTileBytes;   // [kStages][128][D]
-  unsigned char* sOnes = sK + kStages * L::kTileBytes;     // [128][D]
+  unsigned char* sK = smem + 2 * chunks * L::kTileBytes;   // [stages][128][D]
+  unsigned char* sOnes = sK + stages * L::kTileBytes;      // [128][D]
+  float* xchg = reinterpret_cast<float*>(sOnes + L::kTileBytes);  // [2][128][D + 1]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -680,22 +845,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (p.N + kTile - 1) / kTile;
   const int t_begin = blockIdx.x * p.tiles_per_cta;
   const int T = max(0, min(n_tiles, t_begin + p.tiles_per_cta) - t_begin);
-  // slot k takes local tiles k, k+2, ...; each tile runs `chunks` route blocks
+  // Two schedules. With M <= 64 routes (`pairs`) a step of slot k holds two
+  // token tiles, one per column half: step u of slot k takes tiles 2g and
+  // 2g + 1 with g = 2u + k, every half its own tile over all M routes, so a
+  // half's accumulator is a whole output row. Otherwise slot k takes local
+  // tiles k, k+2, ..., each in `chunks` steps of 128 routes, and the two
+  // halves (routes 0-63 and 64-127 of a block) are merged per token at the
+  // end of the tile.
+  const bool pairs = p.M <= 64;
   int steps[2];
-  for (int k = 0; k < 2; ++k) steps[k] = T > k ? ((T - k + 1) / 2) * chunks : 0;
+  for (int k = 0; k < 2; ++k) {
+    if (pairs) {
+      const int G = (T + 1) / 2;
+      steps[k] = G > k ? (G - k + 1) / 2 : 0;
+    } else {
+      steps[k] = T > k ? ((T - k + 1) / 2) * chunks : 0;
+    }
+  }
+  const int umax = max(steps[0], steps[1]);
+  // local token tile of half hf of slot k's step u (may be past T in pairs mode)
+  auto tile_of = [&](int k, int u, int hf) { return pairs ? 2 * (2 * u + k) + hf : k + 2 * (u / chunks); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], 1);
+      mbar_init(&sh.empty[s], pairs ? 1 : 2);  // one release per issuing thread that reads the tile
     }
     mbar_init(&sh.q_full, 1);
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(&sh.s_full[k], 1);
-      mbar_init(&sh.p_full[k], 128);
-      mbar_init(&sh.o_full[k], 1);
-    }
-    mbar_init(&sh.drain, 1);
+    for (int k = 0; k < 2; ++k)
+      for (int hf = 0; hf < 2; ++hf) {
+        mbar_init(&sh.s_full[k][hf], 1);
+        mbar_init(&sh.p_full[k][hf], 4);
+        mbar_init(&sh.o_full[k][hf], 1);
+      }
+    mbar_init(&sh.drain, 4);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -703,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&sh.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 4) fill_ones<D>(sOnes, threadIdx.x - 128, 256);
+  if (warp >= kWarpSoftmax && warp < kWarpSoftmax + 8) fill_ones<D>(sOnes, threadIdx.x - 32 * kWarpSoftmax, 256);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -722,99 +905,161 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int issued = 0;
       for (int t = 0; t < T; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages && !wait_or_abort(sh, &sh.empty[s], ((t / kStages) - 1) & 1)) break;
+        const int s = t % stages;
+        if (t >= stages && !wait_or_abort(sh, &sh.empty[s], ((t / stages) - 1) & 1)) break;
         mbar_arrive_expect_tx(&sh.full[s], L::kTileBytes);
         tma_load_3d(sK + s * L::kTileBytes, &tm_k, &sh.full[s], 0, (t_begin + t) * kTile, bh);
         issued = t + 1;
       }
       if (*(volatile int*)&sh.abort) {
-        for (int t = max(0, issued - kStages); t < issued; ++t)
-          mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, kWaitLimit);
+        for (int t = max(0, issued - stages); t < issued; ++t)
+          mbar_wait(&sh.full[t % stages], (t / stages) & 1, kWaitLimit);
         mbar_wait(&sh.q_full, 0, kWaitLimit);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp < kWarpNorm) {
     if (lane == 0) {
+      const int kk = (warp - kWarpIssue) >> 1, hf = (warp - kWarpIssue) & 1;
       const uint32_t aQ = smem_u32(sQ), aZ = smem_u32(sZ), aOnes = smem_u32(sOnes);
       const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
-      // step u of slot k: local tile k + 2*(u / chunks), route block u % chunks
-      auto issue_s = [&](int k, int u) -> bool {
-        const int t = k + 2 * (u / chunks), ch = u % chunks;
-        const int s = t % kStages;
-        if (ch == 0) {
-          if (!wait_or_abort(sh, &sh.full[s], (t / kStages) & 1)) return false;
-          tc_fence_after();
-        }
-        const int width = min(kTile, p.M - ch * kTile);
-        const uint32_t aK = smem_u32(sK + s * L::kTileBytes);
+      // scores of the half for slot kk's step u: pairs mode, all M routes of
+      // the half's own tile; otherwise routes 64hf .. 64hf+63 of block u % chunks
+      auto issue_s = [&](int u) -> bool {
+        const int t = tile_of(kk, u, hf), ch = pairs ? 0 : u % chunks;
+        if (t < T) {
+          const int s = t % stages;
+          if (ch == 0) {
+            if (!wait_or_abort(sh, &sh.full[s], (t / stages) & 1)) return false;
+            tc_fence_after();
+          }
+          const int width = pairs ? p.M : min(kTile, p.M - ch * kTile) - 64 * hf;
+          if (width > 0) {
+            const uint32_t aK = smem_u32(sK + s * L::kTileBytes);
+            const uint32_t bQ = aQ + ch * L::kTileBytes + (pairs ? 0 : hf * 64 * L::kRowBytes);
 #pragma unroll
-        for (int q = 0; q < D / 16; ++q)
-          mma_ss(tmem + k * kSlotCols, L::kmajor(aK, q), L::kmajor(aQ + ch * L::kTileBytes, q),
-                 idesc_bf16(128, width, false, false), q > 0);
-        if (ch == chunks - 1) mma_commit(&sh.empty[s]);
-        mma_commit(&sh.s_full[k]);
+            for (int q = 0; q < D / 16; ++q)
+              mma_ss(tmem + kk * kSlotCols + 64 * hf, L::kmajor(aK, q), L::kmajor(bQ, q),
+                     idesc_bf16(128, min(width, 64), false, false), q > 0);
+          }
+          if (ch == chunks - 1) mma_commit(&sh.empty[s]);
+        }
+        mma_commit(&sh.s_full[kk][hf]);
         return true;
       };
-      auto issue_pv = [&](int k, int u) {
-        const int ch = u % chunks;
-        const int width = min(kTile, p.M - ch * kTile);
+      // O_hf += P_hf [Z | 1] over the half's route slices
+      auto issue_pv = [&](int u) {
+        if (tile_of(kk, u, hf) >= T) return;
+        const int ch = pairs ? 0 : u % chunks;
+        const int nsl = pairs ? p.M / 16 : min(4, min(kTile, p.M - ch * kTile) / 16 - 4 * hf);
+        const int sl0 = pairs ? 0 : 4 * hf;  // first route slice of the half
         const uint32_t zc = aZ + ch * L::kTileBytes;
-        for (int kk = 0; kk < width / 16; ++kk)
-          mma_ts(tmem + k * kSlotCols + kColO, tmem + k * kSlotCols + kColP + kk * 8, L::values1(zc, aOnes, kk), idO,
-                 (ch > 0 || kk > 0));
-        if (ch == chunks - 1) mma_commit(&sh.o_full[k]);
+        const uint32_t dO = tmem + kk * kSlotCols + kColO + hf * L::kNo;
+        for (int i = 0; i < nsl; ++i)
+          mma_ts(dO, tmem + kk * kSlotCols + 64 * hf + i * 8, L::values1(zc, aOnes, sl0 + i), idO,
+                 (ch > 0 || i > 0));
       };
-      bool ok = wait_or_abort(sh, &sh.q_full, 0);
-      for (int k = 0; ok && k < 2; ++k)
-        if (steps[k] > 0) ok = issue_s(k, 0);
-      const int umax = max(steps[0], steps[1]);
-      for (int u = 0; ok && u < umax; ++u) {
-        for (int k = 0; ok && k < 2; ++k) {
-          if (u >= steps[k]) continue;
-          if (!wait_or_abort(sh, &sh.p_full[k], u & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(k, u);
-          if (u + 1 < steps[k]) ok = issue_s(k, u + 1);
-        }
+      bool ok = steps[kk] > 0 && wait_or_abort(sh, &sh.q_full, 0);
+      if (ok) ok = issue_s(0);
+      for (int u = 0; ok && u < steps[kk]; ++u) {
+        if (!wait_or_abort(sh, &sh.p_full[kk][hf], u & 1)) break;
+        tc_fence_after();
+        issue_pv(u);
+        if (u + 1 < steps[kk]) ok = issue_s(u + 1);
+        else mma_commit(&sh.o_full[kk][hf]);
       }
       mma_commit(&sh.drain);
       mbar_wait(&sh.drain, 0, kWaitLimit);
     }
-  } else if (warp >= 4) {
-    const int k = (warp - 4) >> 2;
-    const int row = (threadIdx.x - 128) & 127;
+  } else if (warp >= kWarpSoftmax && warp < kWarpSoftmax + 8) {
+    const int tid = threadIdx.x - 32 * kWarpSoftmax;  // 0..255
+    const int hf = tid >> 7;
+    const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t tS = tmem + lane_base + k * kSlotCols;
-    const uint32_t tO = tS + kColO;
     const float c = rsqrtf((float)D) * kLog2e;
-    float m = -INFINITY;
-    for (int u = 0; u < steps[k]; ++u) {
-      const int ch = u % chunks;
-      if (!wait_or_abort(sh, &sh.s_full[k], u & 1)) break;
-      tc_fence_after();
-      if (ch == 0) m = -INFINITY;
-      const int width = min(kTile, p.M - ch * kTile);
-      if (width > 64) softmax_step<D, kTile>(tS, tS + kColP, tO, width, c, m, ch > 0);
-      else if (width > 32) softmax_step<D, 64>(tS, tS + kColP, tO, width, c, m, ch > 0);
-      else softmax_step<D, 32>(tS, tS + kColP, tO, width, c, m, ch > 0);
-      tc_fence_before();
-      mbar_arrive(&sh.p_full[k]);
-      if (ch == chunks - 1) {
-        const int t = k + 2 * (u / chunks);
-        if (!wait_or_abort(sh, &sh.o_full[k], (u / chunks) & 1)) break;
-        tc_fence_after();
-        float y[D];
-        const float l = load_acc<D>(tO, y);
-        const int n = (t_begin + t) * kTile + row;
-        if (n < p.N) {
-          const float inv = 1.f / l;
+    float r[2] = {-INFINITY, -INFINITY}, ro[2] = {-INFINITY, -INFINITY};
+    bool acc[2] = {false, false};
+    // out = O / rowsum of this half's accumulator, for its own token tile
+    // (pairs mode: no exchange)
+    auto emit_own = [&](int k, int u, bool live) {
+      const int t = tile_of(k, u, hf);
+      if (!live || t >= T) return;
+      float z[D];
+      const float l = load_acc<D>(tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo, z);
+      const int tok = (t_begin + t) * kTile + row;
+      if (tok < p.N) {
+        const float inv = 1.f / l;
 #pragma unroll
-          for (int d = 0; d < D; ++d) y[d] *= inv;
-          store_row<D>(p.out + ((size_t)bh * p.N + n) * D, y);
-        }
-        tc_fence_before();
+        for (int d = 0; d < D; ++d) z[d] *= inv;
+        store_row<D>(p.out + ((size_t)bh * p.N + tok) * D, z);
       }
+    };
+    // out = the two halves' (L, Z) merged, for the token tile of slot k's step
+    // u. Every softmax thread calls it at the same points of the schedule,
+    // also after a failed wait (`live` false), so that the exchange barrier
+    // inside always completes.
+    auto emit_merged = [&](int k, int u, bool live) {
+      const int t = tile_of(k, u, 0);
+      float z[D];
+      const float l = load_acc<D>(tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo, z);
+      const bool any = live && acc[k] && l > 0.f;
+      const float lg = any ? ro[k] + __log2f(l) : -INFINITY;  // exp2 units
+      const float inv = any ? 1.f / l : 0.f;
+      float* xr = xchg + (k * 128 + row) * (D + 1);
+      if (hf == 1) {
+        xr[0] = lg;
+#pragma unroll
+        for (int d = 0; d < D; ++d) xr[1 + d] = z[d] * inv;
+      }
+      softmax_groups_sync();
+      if (hf == 0 && live) {
+        const float lb = xr[0];
+        const float m = fmaxf(lg, lb);
+        const float wa = lg == -INFINITY ? 0.f : exp2f(lg - m);
+        const float wb = lb == -INFINITY ? 0.f : exp2f(lb - m);
+        const float inv_w = 1.f / (wa + wb);
+        const int tok = (t_begin + t) * kTile + row;
+        if (tok < p.N) {
+#pragma unroll
+          for (int d = 0; d < D; ++d) z[d] = (wa * z[d] * inv + wb * xr[1 + d]) * inv_w;
+          store_row<D>(p.out + ((size_t)bh * p.N + tok) * D, z);
+        }
+      }
+    };
+    bool ok = true;
+    for (int u = 0; u < umax; ++u) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (u >= steps[k]) continue;
+        const uint32_t tS = tmem + lane_base + k * kSlotCols + 64 * hf;
+        const uint32_t tO = tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo;
+        const int ch = pairs ? 0 : u % chunks;
+        ok = ok && wait_or_abort(sh, &sh.s_full[k][hf], u & 1);
+        tc_fence_after();
+        if (ch == 0) {
+          // the previous tile's products are in: its output goes out before
+          // this step's products overwrite the accumulators
+          if (u > 0) {
+            if (pairs) emit_own(k, u - 1, ok);
+            else emit_merged(k, u - 1, ok);
+          }
+          r[k] = -INFINITY;
+          acc[k] = false;
+        }
+        if (!ok) continue;
+        const int valid = pairs ? (tile_of(k, u, hf) < T ? p.M : 0) : min(kTile, p.M - ch * kTile) - 64 * hf;
+        if (valid > 0) softmax_half(tS, min(valid, 64), c, r[k]);
+        finish_half<D>(&sh.p_full[k][hf], tO, r[k], ro[k], acc[k]);
+        if (valid > 0) acc[k] = true;
+      }
+    }
+    // the last tile of each slot
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (steps[k] == 0) continue;
+      const bool done = ok && wait_or_abort(sh, &sh.o_full[k][hf], 0);
+      tc_fence_after();
+      if (pairs) emit_own(k, steps[k] - 1, done);
+      else emit_merged(k, steps[k] - 1, done);
     }
   }
   tc_fence_before();
@@ -858,16 +1103,16 @@ bool make_map(CUtensorMap* map, const void* base, int D, int rows, int planes, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
-size_t split_smem(bool synth) {
-  const size_t stage = synth ? Layout<D>::kTileBytes : 2 * Layout<D>::kTileBytes;
-  return 1024 + 3 * (size_t)Layout<D>::kTileBytes + kStages * stage;
+template <int D, bool kSynth>
+size_t split_smem() {
+  const size_t stage = kSynth ? Layout<D>::kTileBytes : 2 * Layout<D>::kTileBytes;
+  return 1024 + 3 * (size_t)Layout<D>::kTileBytes + split_stages<D, kSynth>() * stage;
 }
 
 template <int D>
 size_t decode_smem(int M) {
   const int chunks = (M + kTile - 1) / kTile;
-  return 1024 + (2 * chunks + kStages + 1) * (size_t)Layout<D>::kTileBytes;
+  return 1024 + (2 * chunks + decode_stages<D>(M) + 1) * (size_t)Layout<D>::kTileBytes + decode_xchg_bytes<D>();
 }
 
 template <int D>
@@ -900,7 +1145,7 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
     a.out = static_cast<__nv_bfloat16*>(ws.q);
     a.dbg_a = pr.dbg_qd;
     a.dbg_b = pr.dbg_q;
-    const size_t smem = split_smem<D>(true);
+    const size_t smem = split_smem<D, true>();
     *failed = "cudaFuncSetAttribute(synthesis)";
     if ((e = cudaFuncSetAttribute(split_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)smem)) != cudaSuccess)
@@ -917,7 +1162,7 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
     a.out = static_cast<__nv_bfloat16*>(ws.z);
     a.dbg_a = pr.dbg_z;
     a.dbg_b = pr.dbg_l;
-    const size_t smem = split_smem<D>(false);
+    const size_t smem = split_smem<D, false>();
     *failed = "cudaFuncSetAttribute(encode)";
     if ((e = cudaFuncSetAttribute(split_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)smem)) != cudaSuccess)
@@ -931,6 +1176,7 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
   {
     DecodeParams d{};
     d.N = pr.N; d.M = pr.M; d.tiles_per_cta = pl.decode_tiles_per_cta;
+    d.stages = decode_stages<D>(pr.M);
     d.out = static_cast<__nv_bfloat16*>(pr.out);
     const size_t smem = decode_smem<D>(pr.M);
     *failed = "cudaFuncSetAttribute(decode)";
