@@ -145,6 +145,9 @@ struct Layout {
   static __device__ __forceinline__ uint64_t values1(uint32_t base, uint32_t ones, int kk) {
     return sdesc(base + kk * 2 * kAtom, ones - base, kAtom, kSwz);
   }
+  // A descriptor moved `bytes` further (the start field holds address / 16;
+  // shared-memory addresses stay below 2^18, so no carry leaves the field).
+  static __device__ __forceinline__ uint64_t adv(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
   // Byte offset of logical 16-byte chunk `c` of row `r` in a swizzled tile.
   static __device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
     const int x = D == 32 ? ((r >> 1) & 3) : ((r >> 2) & 1);
@@ -505,6 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto ready = [&](int t) -> bool {
         return wait_or_abort(sh, kSynth ? &sh.norm[t % kStages] : &sh.full[t % kStages], (t / kStages) & 1);
       };
+      // key descriptor of the half's rows in stage 0; a stage is kStageBytes further
+      const uint64_t dK0 = L::kmajor(smem_u32(sStage) + rows_off, 0);
+      auto key_desc = [&](int t) { return L::adv(dK0, (t % kStages) * kStageBytes); };
       // scores of the half's 64 token columns of slot k, step j; the latent
       // queries (A) are read from TMEM, the keys (B) from the staged tile
       auto issue_s = [&](int k, int j) -> bool {
@@ -516,19 +522,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool has_b = t + 1 < T;
           if (has_b && !ready(t + 1)) return false;
           tc_fence_after();
+          const uint64_t ka = key_desc(t);
 #pragma unroll
           for (int q = 0; q < D / 16; ++q)
-            mma_ts_masked(dS, tQ + q * 8, L::kmajor(stage_addr(t) + rows_off, q), idS, q > 0, kLo, kLo, kAll, kAll);
+            mma_ts_masked(dS, tQ + q * 8, L::adv(ka, 32 * q), idS, q > 0, kLo, kLo, kAll, kAll);
           if (has_b) {
+            const uint64_t kb = key_desc(t + 1);
 #pragma unroll
             for (int q = 0; q < D / 16; ++q)
-              mma_ts_masked(dS, tQ + q * 8, L::kmajor(stage_addr(t + 1) + rows_off, q), idS, q > 0, kAll, kAll, kLo,
-                            kLo);
+              mma_ts_masked(dS, tQ + q * 8, L::adv(kb, 32 * q), idS, q > 0, kAll, kAll, kLo, kLo);
           }
         } else {
           tc_fence_after();
+          const uint64_t ka = key_desc(t);
 #pragma unroll
-          for (int q = 0; q < D / 16; ++q) mma_ts(dS, tQ + q * 8, L::kmajor(stage_addr(t) + rows_off, q), idS, q > 0);
+          for (int q = 0; q < D / 16; ++q) mma_ts(dS, tQ + q * 8, L::adv(ka, 32 * q), idS, q > 0);
         }
         mma_commit(&sh.s_full[k][hf]);
         return true;
@@ -539,24 +547,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dO = tmem + k * kSlotCols + kColO + hf * L::kNo;
         const uint32_t aP = tmem + k * kSlotCols + 64 * hf;
         const int t = slot_tile(sp, k, j);
-        const uint32_t vA = stage_addr(t) + (kSynth ? 0 : L::kTileBytes);
+        const uint32_t first = j > 0 ? 1u : 0u;
+        const uint64_t va = L::values1(stage_addr(t) + (kSynth ? 0 : L::kTileBytes), aOnes, 4 * hf);
         if (sp.mode == kLanes) {
           const bool has_b = t + 1 < T;
-          const uint32_t vB = stage_addr(t + 1) + (kSynth ? 0 : L::kTileBytes);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            mma_ts_masked(dO, aP + i * 8, L::values1(vA, aOnes, 4 * hf + i), idO, (j > 0 || i > 0), kLo, kLo, kAll,
+            mma_ts_masked(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kLo, kLo, kAll,
                           kAll);
           if (has_b) {
+            const uint64_t vb = L::values1(stage_addr(t + 1) + (kSynth ? 0 : L::kTileBytes), aOnes, 4 * hf);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              mma_ts_masked(dO, aP + i * 8, L::values1(vB, aOnes, 4 * hf + i), idO, (j > 0 || i > 0), kAll, kAll,
-                            kLo, kLo);
+              mma_ts_masked(dO, aP + i * 8, L::adv(vb, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kAll, kAll, kLo,
+                            kLo);
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            mma_ts(dO, aP + i * 8, L::values1(vA, aOnes, 4 * hf + i), idO, (j > 0 || i > 0));
+          for (int i = 0; i < 4; ++i) mma_ts(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
         }
       };
       // the stage(s) of the step can be refilled once this thread's products
@@ -924,6 +932,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
       // scores of the half for slot kk's step u: pairs mode, all M routes of
       // the half's own tile; otherwise routes 64hf .. 64hf+63 of block u % chunks
+      // descriptors built once; an MMA moves them with one add (a thread
+      // spends its issue slots on every instruction between MMAs)
+      const uint64_t dK0 = L::kmajor(smem_u32(sK), 0);
+      const uint64_t dQ0 = L::kmajor(aQ + (pairs ? 0u : hf * 64u * L::kRowBytes), 0);
+      const uint32_t idS64 = idesc_bf16(128, 64, false, false);
+      const uint32_t dS = tmem + kk * kSlotCols + 64 * hf;
+      const uint32_t dO = tmem + kk * kSlotCols + kColO + hf * L::kNo;
+      // scores of the half for slot kk's step u: pairs mode, all M routes of
+      // the half's own tile; otherwise routes 64hf .. 64hf+63 of block u % chunks
       auto issue_s = [&](int u) -> bool {
         const int t = tile_of(kk, u, hf), ch = pairs ? 0 : u % chunks;
         if (t < T) {
@@ -934,12 +951,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int width = pairs ? p.M : min(kTile, p.M - ch * kTile) - 64 * hf;
           if (width > 0) {
-            const uint32_t aK = smem_u32(sK + s * L::kTileBytes);
-            const uint32_t bQ = aQ + ch * L::kTileBytes + (pairs ? 0 : hf * 64 * L::kRowBytes);
+            const uint64_t a = L::adv(dK0, s * L::kTileBytes), b = L::adv(dQ0, ch * L::kTileBytes);
+            const uint32_t id = width >= 64 ? idS64 : idesc_bf16(128, width, false, false);
 #pragma unroll
-            for (int q = 0; q < D / 16; ++q)
-              mma_ss(tmem + kk * kSlotCols + 64 * hf, L::kmajor(aK, q), L::kmajor(bQ, q),
-                     idesc_bf16(128, min(width, 64), false, false), q > 0);
+            for (int q = 0; q < D / 16; ++q) mma_ss(dS, L::adv(a, 32 * q), L::adv(b, 32 * q), id, q > 0);
           }
           if (ch == chunks - 1) mma_commit(&sh.empty[s]);
         }
@@ -953,10 +968,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nsl = pairs ? p.M / 16 : min(4, min(kTile, p.M - ch * kTile) / 16 - 4 * hf);
         const int sl0 = pairs ? 0 : 4 * hf;  // first route slice of the half
         const uint32_t zc = aZ + ch * L::kTileBytes;
-        const uint32_t dO = tmem + kk * kSlotCols + kColO + hf * L::kNo;
-        for (int i = 0; i < nsl; ++i)
-          mma_ts(dO, tmem + kk * kSlotCols + 64 * hf + i * 8, L::values1(zc, aOnes, sl0 + i), idO,
-                 (ch > 0 || i > 0));
+        const uint64_t v = L::values1(zc, aOnes, sl0);
+        const uint32_t aP = tmem + kk * kSlotCols + 64 * hf;
+        const uint32_t first = ch > 0 ? 1u : 0u;
+        if (nsl == 4) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mma_ts(dO, aP + i * 8, L::adv(v, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
+        } else {
+          for (int i = 0; i < nsl; ++i) mma_ts(dO, aP + i * 8, L::adv(v, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
+        }
       };
       bool ok = steps[kk] > 0 && wait_or_abort(sh, &sh.q_full, 0);
       if (ok) ok = issue_s(0);
