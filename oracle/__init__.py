@@ -3,10 +3,13 @@
 Imported by tests, the package smoke check and the benchmark's CPU-baseline
 leg; never by the library path.
 """
-from .flarepp_oracle import (EPS, decode, encode, encode_partial, forward, forward_head,
-                             logsumexp_rows, lse_merge, n0, routing_queries, sdpa,
-                             softmax_rows, synthesis, w_eff)
+from .flarepp_oracle import (EPS, decode, encode, encode_partial, flare_forward,
+                             flare_forward_head, forward, forward_head, forward_simplified,
+                             forward_unshared, logsumexp_rows, lse_merge, n0, routing_queries,
+                             sdpa, softmax_rows, synthesis, synthesis_simplified,
+                             synthesis_unshared, w_eff)
 
-__all__ = ["EPS", "decode", "encode", "encode_partial", "forward", "forward_head",
-           "logsumexp_rows", "lse_merge", "n0", "routing_queries", "sdpa", "softmax_rows",
-           "synthesis", "w_eff"]
+__all__ = ["EPS", "decode", "encode", "encode_partial", "flare_forward", "flare_forward_head",
+           "forward", "forward_head", "forward_simplified", "forward_unshared", "logsumexp_rows",
+           "lse_merge", "n0", "routing_queries", "sdpa", "softmax_rows", "synthesis",
+           "synthesis_simplified", "synthesis_unshared", "w_eff"]

@@ -16,6 +16,9 @@ routing", arXiv 2608.11519 v2):
 * Q = N0(Q^f) + g * Q^d (eq. 7 / eq. 15).
 * Z = SDPA(Q, K, V), L = log-sum-exp of the encode scores (eq. 8, B.2 eq. 25).
 * Y = SDPA(K, Q, Z), softmax over the M routes (eq. 8, Figure 1 caption).
+* the mixer variants the paper defines beside it, at the end of the module:
+  FLARE (Section 3.1 eq. 3), separate synthesis values (Appendix A.1 eq. 11)
+  and simplified FLARE++ (Appendix A.8 eq. 20).
 
 Readings where the paper is silent (each one is also listed in the design
 notes of the repository):
@@ -194,3 +197,97 @@ def w_eff(q: np.ndarray, k: np.ndarray) -> np.ndarray:
     w_enc = softmax_rows(s)
     w_dec = softmax_rows(s.T)
     return w_dec @ w_enc
+
+
+# ------------------------------------------------------------------ variants
+# The FLARE++ paper also defines the mixer it improves on (FLARE, Section 3.1
+# eq. 2-3), the general form with a separate synthesis value projection
+# (Appendix A.1 eq. 11) and the simplified variant (Appendix A.8 eq. 20).
+# Readings where the paper leaves a step open (also in the design notes):
+#
+# 6. FLARE's learned queries Q_h are used as given; the caller owns any
+#    normalisation of Q_h and of K.
+# 7. In the general form the library applies N0 to the synthesis keys only;
+#    the separate values V~ are used as given. V~ = N0(Ks_raw) is the default
+#    shared configuration.
+# 8. In the simplified variant the learned-scale normalisations N_a of the
+#    seeds and of the synthesis keys are applied by the caller (as for K in
+#    the main mixer); V~ is unnormalised; there is no reference and no gate,
+#    so Q = Q^d.
+
+
+def flare_forward_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: int | None = None) -> dict:
+    """FLARE for one (batch, head): Z = SDPA(Q_h, K, V), Y = SDPA(K, Q_h, Z)
+    (Section 3.1 eq. 3). q [M, D] is the head's learned query set."""
+    z, lse = encode(q, k, v, rows=rows)
+    y = decode(k, q, z, rows=rows)
+    return {"Q": np.asarray(q, dtype=np.float64), "Z": z, "L": lse, "Y": y}
+
+
+def flare_forward(Q, K, V, rows: int | None = None) -> dict:
+    """FLARE over all batches and heads. Q [H,M,D]; K, V [B,H,N,D].
+
+    Returns Q, Z [B,H,M,D], L [B,H,M] and Y [B,H,N,D] (float64)."""
+    B, H, N, D = K.shape
+    M = Q.shape[1]
+    res = {"Q": np.empty((B, H, M, D)), "Z": np.empty((B, H, M, D)), "L": np.empty((B, H, M)),
+           "Y": np.empty((B, H, N, D))}
+    for b in range(B):
+        for h in range(H):
+            r = flare_forward_head(Q[h], K[b, h], V[b, h], rows=rows)
+            for key in res:
+                res[key][b, h] = r[key]
+    return res
+
+
+def synthesis_unshared(qseed_h: np.ndarray, ks_raw_bh: np.ndarray, vs_bh: np.ndarray,
+                       rows: int | None = None) -> np.ndarray:
+    """Q^d = SDPA(Qseed, N0(Ks_raw), V~) with a separate value projection V~
+    (Appendix A.1 eq. 11, keys normalised as in Section 3.2 eq. 5)."""
+    return sdpa(qseed_h, n0(ks_raw_bh), vs_bh, rows=rows)
+
+
+def synthesis_simplified(qseed_h: np.ndarray, ks_bh: np.ndarray, vs_bh: np.ndarray,
+                         rows: int | None = None) -> np.ndarray:
+    """Q = Q^d = SDPA(N_a(Q~), N_a(K~), V~) (Appendix A.8 eq. 20), with the
+    N_a already applied to ``qseed_h`` and ``ks_bh`` by the caller."""
+    return sdpa(qseed_h, ks_bh, vs_bh, rows=rows)
+
+
+def _route(q, k, v, rows):
+    z, lse = encode(q, k, v, rows=rows)
+    return z, lse, decode(k, q, z, rows=rows)
+
+
+def forward_unshared(K, V, Ks_raw, Vs, Qseed, Qf, gate, rows: int | None = None) -> dict:
+    """FLARE++ with separate synthesis values (eq. 11): Q^d from
+    ``synthesis_unshared``, then Q = N0(Q^f) + g Q^d and eq. 8 as in ``forward``.
+    Vs [B,H,N,D]; the other arguments as in ``forward``."""
+    B, H, N, D = K.shape
+    M = Qseed.shape[1]
+    res = {"Qd": np.empty((B, H, M, D)), "Q": np.empty((B, H, M, D)),
+           "Z": np.empty((B, H, M, D)), "L": np.empty((B, H, M)), "Y": np.empty((B, H, N, D))}
+    for b in range(B):
+        for h in range(H):
+            qd = synthesis_unshared(Qseed[h], Ks_raw[b, h], Vs[b, h], rows=rows)
+            q = routing_queries(Qf[h], qd, gate[h])
+            z, lse, y = _route(q, K[b, h], V[b, h], rows)
+            for key, val in (("Qd", qd), ("Q", q), ("Z", z), ("L", lse), ("Y", y)):
+                res[key][b, h] = val
+    return res
+
+
+def forward_simplified(K, V, Ks, Vs, Qseed, rows: int | None = None) -> dict:
+    """Simplified FLARE++ (eq. 20): Q = SDPA(Qseed, Ks, Vs), then eq. 8.
+    Ks, Vs [B,H,N,D] as used (N_a applied to Ks by the caller); Qseed [H,M,D]."""
+    B, H, N, D = K.shape
+    M = Qseed.shape[1]
+    res = {"Q": np.empty((B, H, M, D)), "Z": np.empty((B, H, M, D)), "L": np.empty((B, H, M)),
+           "Y": np.empty((B, H, N, D))}
+    for b in range(B):
+        for h in range(H):
+            q = synthesis_simplified(Qseed[h], Ks[b, h], Vs[b, h], rows=rows)
+            z, lse, y = _route(q, K[b, h], V[b, h], rows)
+            for key, val in (("Q", q), ("Z", z), ("L", lse), ("Y", y)):
+                res[key][b, h] = val
+    return res

@@ -26,6 +26,11 @@ experiments, as synthetic stand-ins (no dataset is used):
 
 Seeds Qseed and Qf are N(0,1)/sqrt(D) of shape [H, M, D]; the gate is
 U(0,1) per head (already the post-sigmoid value g).
+
+The mixer variants take two more tensors (``variant_inputs``): separate
+synthesis values Vs [B, H, N, D], drawn like the other token tensors, and
+FLARE's learned queries [H, M, D], N(0,1) (unit RMS rows, the magnitude of
+N0(Qf) that the default mixer routes with).
 """
 from __future__ import annotations
 
@@ -42,6 +47,7 @@ _C2 = np.uint64(0x94D049BB133111EB)
 # sub-stream ids of the tensors of one workload
 STREAM_K, STREAM_V, STREAM_KS, STREAM_QSEED, STREAM_QF, STREAM_GATE = 1, 2, 3, 4, 5, 6
 STREAM_AUX = 7  # tokens ids, points, low-rank factors and similar structure
+STREAM_VS, STREAM_QLAT = 8, 9  # separate synthesis values; FLARE's learned queries
 
 _CHUNK = 1 << 18
 
@@ -158,6 +164,8 @@ class Workload:
     Qf: np.ndarray
     gate: np.ndarray
     bits: dict = field(default_factory=dict)
+    structure: str | None = None  # value structure and seed it was drawn with
+    seed: int | None = None
 
     def device_arrays(self) -> dict:
         """Host arrays in the layout the library takes (uint16 bits for bf16)."""
@@ -253,7 +261,7 @@ def make(shape: Shape, dtype: str = "bf16", structure: str = "iid", seed: int = 
             bits[k] = hb
     gate = uniform(seed, STREAM_GATE, s.H).astype(np.float32)
     return Workload(name, s, dtype, vals["K"], vals["V"], vals["Ks_raw"], vals["Qseed"],
-                    vals["Qf"], gate, bits)
+                    vals["Qf"], gate, bits, structure, seed)
 
 
 def _latents(s: Shape, seed: int, qseed_scale: float = 1.0) -> dict:
@@ -304,3 +312,32 @@ def config(name: str, **overrides) -> Workload:
     dtype = overrides.pop("dtype", dtype)
     seed = overrides.pop("seed", seed)
     return make(Shape(**dims), dtype, structure, seed, name=name, **overrides)
+
+
+def variant_inputs(wl: Workload) -> dict:
+    """The extra inputs of the mixer variants for workload ``wl`` (same shape,
+    dtype, structure and seed): ``Vs`` [B,H,N,D] and ``Qlat`` [H,M,D] as float32
+    values exactly representable in the dtype, with ``Vs_bits``/``Qlat_bits``
+    (uint16) for bf16."""
+    s = wl.shape
+    if wl.structure is None:
+        raise ValueError("variant inputs need a drawn workload (not from_arrays)")
+    seed = wl.seed
+    gen = _STRUCTURES[wl.structure]
+    vs = np.empty((s.B, s.H, s.N, s.D), dtype=np.float32)
+    vb = np.empty((s.B, s.H, s.N, s.D), dtype=np.uint16)
+    for b in range(s.B):
+        for h in range(s.H):
+            hb, hv = _round(gen(seed, STREAM_VS, s, b, h), wl.dtype)
+            vs[b, h] = hv
+            if hb is not None:
+                vb[b, h] = hb
+    ql = normal(seed, STREAM_QLAT, s.H * s.M * s.D).reshape(s.H, s.M, s.D)
+    qb, qv = _round(ql, wl.dtype)
+    out = {"Vs": vs, "Qlat": qv}
+    if wl.dtype == "bf16":
+        out["Vs_bits"] = vb
+        out["Qlat_bits"] = qb
+    return out
+
+
