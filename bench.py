@@ -116,24 +116,37 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- our path
-def upload(wl, torch, device):
+# inputs each mixer variant reads (the library refuses others)
+VARIANT_INPUTS = {
+    "flarepp": ("K", "V", "Ks_raw", "Qseed", "Qf", "gate"),
+    "unshared": ("K", "V", "Ks_raw", "Vs", "Qseed", "Qf", "gate"),
+    "simplified": ("K", "V", "Ks_raw", "Vs", "Qseed"),
+    "flare": ("Qlat", "K", "V"),
+}
+
+
+def upload(wl, torch, device, variant="flarepp"):
+    names = VARIANT_INPUTS[variant]
+    ex = workloads.variant_inputs(wl) if ("Vs" in names or "Qlat" in names) else {}
     out = {}
-    for k in ("K", "V", "Ks_raw", "Qseed", "Qf"):
-        if wl.dtype == "bf16":
-            a = torch.from_numpy(np.ascontiguousarray(wl.bits[k]).view(np.int16)).view(torch.bfloat16)
+    for k in names:
+        if k == "gate":
+            out[k] = torch.from_numpy(wl.gate)
+        elif wl.dtype == "bf16":
+            bits = ex[k + "_bits"] if k in ex else wl.bits[k]
+            out[k] = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
         else:
-            a = torch.from_numpy(np.ascontiguousarray(getattr(wl, k)))
-        out[k] = a
-    out["gate"] = torch.from_numpy(wl.gate)
+            out[k] = torch.from_numpy(np.ascontiguousarray(ex[k] if k in ex else getattr(wl, k)))
     dev = {k: v.to(device) for k, v in out.items()}
     host = {k: v.pin_memory() for k, v in out.items()}
     return dev, host
 
 
-def stage_costs(s: workloads.Shape, es: int):
+def stage_costs(s: workloads.Shape, es: int, variant: str = "flarepp"):
     """Algorithmic work of each pass per call: bytes moved, flops, exps.
 
-    Per (token, head): synthesis reads Ks_raw (D elements); encode reads K and
+    Per (token, head): synthesis reads Ks_raw (D elements; 2D with separate
+    values Vs; nothing for FLARE, which has no synthesis); encode reads K and
     V (2D); decode reads K and writes Y (2D). Each pass scores N x M and
     multiplies by a D-wide value: 4*M*D flops and M exponentials per token.
     Latent-sized traffic (Qseed, Qf, Q, Z, partials) is below 1% and not counted.
@@ -141,8 +154,10 @@ def stage_costs(s: workloads.Shape, es: int):
     th = s.B * s.H * s.N
     per_pass_flops = 4.0 * th * s.M * s.D
     per_pass_exps = float(th) * s.M
+    synth = {"flarepp": 1, "unshared": 2, "simplified": 2, "flare": 0}[variant]
     return {
-        "synthesis": {"bytes": th * s.D * es, "flops": per_pass_flops, "exps": per_pass_exps},
+        "synthesis": {"bytes": synth * th * s.D * es, "flops": per_pass_flops * (synth > 0),
+                      "exps": per_pass_exps * (synth > 0)},
         "encode": {"bytes": 2 * th * s.D * es, "flops": per_pass_flops, "exps": per_pass_exps},
         "decode": {"bytes": 2 * th * s.D * es, "flops": per_pass_flops, "exps": per_pass_exps},
     }
@@ -221,15 +236,21 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     wl = workloads.config(args.workload)
     s = wl.shape
-    dev, host = upload(wl, torch, device)
+    dev, host = upload(wl, torch, device, args.variant)
     tdtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     out = torch.empty(s.B, s.H, s.N, s.D, dtype=tdtype, device=device)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
     def step():
-        flarepp.forward(dev["K"], dev["V"], dev["Ks_raw"], dev["Qseed"], dev["Qf"], dev["gate"],
-                        out=out)
+        if args.variant == "flarepp":
+            flarepp.forward(dev["K"], dev["V"], dev["Ks_raw"], dev["Qseed"], dev["Qf"],
+                            dev["gate"], out=out)
+        elif args.variant == "flare":
+            flarepp.flare_forward(dev["Qlat"], dev["K"], dev["V"], out=out)
+        else:
+            flarepp.forward_variant(args.variant, dev["K"], dev["V"], dev["Ks_raw"], dev["Vs"],
+                                    dev["Qseed"], dev.get("Qf"), dev.get("gate"), out=out)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -306,14 +327,16 @@ def run_ours(args, rank, world, local_rank):
     tokens = s.tokens * world
     ms_step = t_max / args.steps
     value = tokens / (ms_step * 1e-3)
-    tflops = s.flops * world / (ms_step * 1e-3) / 1e12
-    costs = stage_costs(s, 2 if wl.dtype == "bf16" else 4)
+    passes = 2 if args.variant == "flare" else 3
+    tflops = s.flops * passes / 3 * world / (ms_step * 1e-3) / 1e12
+    costs = stage_costs(s, 2 if wl.dtype == "bf16" else 4, args.variant)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic (seeded, shapes of the paper's workloads)",
-        "config": {"workload": f"{wl.name}: B={s.B} H={s.H} N={s.N} M={s.M} D={s.D} {wl.dtype}",
+        "config": {"workload": f"{wl.name}: B={s.B} H={s.H} N={s.N} M={s.M} D={s.D} {wl.dtype}"
+                               + ("" if args.variant == "flarepp" else f", {args.variant} mixer"),
                    "global_batch": s.B * world, "seq_len": s.N, "latents": s.M, "head_dim": s.D,
                    "heads": s.H, "parallelism": f"replicas x{world}" if world > 1 else "single",
                    "l2": "512 MB flush before every timed step"},
@@ -324,11 +347,12 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(tokens / (e2e_max * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_max, 4)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": passes * args.steps,
         "impl": "ours",
     }
     rl = line["roofline"]
-    rl["traffic"] = measured_traffic(args.workload, rl["kernel"])
+    rl["traffic"] = (measured_traffic(args.workload, rl["kernel"]) if args.variant == "flarepp"
+                     else None)
     return line
 
 
@@ -346,14 +370,26 @@ def _oracle_job(job):
     returns its wall time. The head's inputs are drawn once per process."""
     import oracle
     from rank_latent_routing_gb300 import workloads as w
-    name, b, h, n_tok = job
+    name, variant, b, h, n_tok = job
     key = (name, b, h)
     if key not in _HEADS:
         _HEADS[key] = w.make_head(name, b, h)
+        if variant != "flarepp":
+            _HEADS[key].update(w.make_variant_head(name, b, h))
     x = _HEADS[key]
+    K, V = x["K"][:n_tok], x["V"][:n_tok]
     t0 = time.perf_counter()
-    oracle.forward_head(x["K"][:n_tok], x["V"][:n_tok], x["Ks_raw"][:n_tok], x["Qseed"],
-                        x["Qf"], x["gate"])
+    if variant == "flarepp":
+        oracle.forward_head(K, V, x["Ks_raw"][:n_tok], x["Qseed"], x["Qf"], x["gate"])
+    elif variant == "flare":
+        oracle.flare_forward_head(x["Qlat"], K, V)
+    else:
+        args = (K[None, None], V[None, None], x["Ks_raw"][:n_tok][None, None],
+                x["Vs"][:n_tok][None, None], x["Qseed"][None])
+        if variant == "unshared":
+            oracle.forward_unshared(*args, x["Qf"][None], np.array([x["gate"]]))
+        else:
+            oracle.forward_simplified(*args)
     return time.perf_counter() - t0
 
 
@@ -361,9 +397,9 @@ class OraclePool:
     """``cores`` spawned processes with one BLAS thread each; each runs whole
     (batch, head) problems of the workload through the unmodified oracle."""
 
-    def __init__(self, name, cores):
+    def __init__(self, name, cores, variant="flarepp"):
         import multiprocessing as mp
-        self.name, self.cores = name, cores
+        self.name, self.cores, self.variant = name, cores, variant
         self.shape = workloads.CONFIGS[name][0]
         s = self.shape
         # each process draws its own heads; keep to `cores` distinct heads
@@ -373,7 +409,8 @@ class OraclePool:
         self.round(min(s.N, 256))  # draw inputs, import modules
 
     def round(self, n_tok):
-        jobs = [(self.name, *self.heads[i % len(self.heads)], n_tok) for i in range(self.cores)]
+        jobs = [(self.name, self.variant, *self.heads[i % len(self.heads)], n_tok)
+                for i in range(self.cores)]
         t0 = time.perf_counter()
         self.pool.map(_oracle_job, jobs, chunksize=1)
         return time.perf_counter() - t0
@@ -387,7 +424,7 @@ def cpu_baseline(args):
     """The oracle's tokens/s on the host cores, on about ``--cpu-seconds`` of
     whole-head problems of the benchmark workload."""
     cores = os.cpu_count() or 1
-    pool = OraclePool(args.workload, cores)
+    pool = OraclePool(args.workload, cores, args.variant)
     s = pool.shape
     done, el = 0, 0.0
     while el < args.cpu_seconds:
@@ -396,7 +433,7 @@ def cpu_baseline(args):
     pool.close()
     rate = done * s.N / s.H / el
     return {"value": round(rate, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} whole (batch, head) problems of {args.workload} (N={s.N}) in "
+            "sample": f"{done} whole (batch, head) {args.variant} problems of {args.workload} (N={s.N}) in "
                       f"{el:.1f} s on {cores} processes x 1 BLAS thread; tokens/s = "
                       "problems x N / H / wall time"}
 
@@ -406,7 +443,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     cores = os.cpu_count() or 1
-    pool = OraclePool(args.workload, cores)
+    pool = OraclePool(args.workload, cores, args.variant)
     s = pool.shape
     budget = 120.0  # seconds for all warm-up and timed steps together
     per_step = max(0.05, budget / max(1, args.steps + args.warmup))
@@ -427,7 +464,8 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, shapes of the paper's workloads)",
-            "config": {"workload": f"{args.workload}: B={s.B} H={s.H} N={s.N} M={s.M} D={s.D}",
+            "config": {"workload": f"{args.workload}: B={s.B} H={s.H} N={s.N} M={s.M} D={s.D}"
+                                   + ("" if args.variant == "flarepp" else f", {args.variant} mixer"),
                        "parallelism": "host cores"},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores,
@@ -446,6 +484,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="pde2d", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--variant", default="flarepp", choices=sorted(VARIANT_INPUTS),
+                    help="mixer: FLARE++ (default), separate synthesis values, simplified "
+                         "FLARE++, or FLARE")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -120,6 +120,66 @@ flarepp_status_t flarepp_forward_static(const void* K, const void* V, const void
                                         void* out, cudaStream_t stream);
 
 /*
+ * The two synthesis variants that the FLARE++ paper defines beside the
+ * default mixer above (Appendix A.1 and A.8), for flarepp_forward_variant.
+ */
+typedef enum {
+  /* The default mixer above: Vs must be NULL (eq. 5-8, eq. 19). */
+  FLAREPP_VARIANT_SHARED = 0,
+  /* The general form with a separate synthesis value projection (Appendix
+   * A.1, eq. 11):  Qd = softmax_N(s Qseed N0(Ks_raw)^T) Vs, then
+   * Q = N0(Qf) + g Qd and eq. 8 as above. Vs [B,H,N,D] is used as given (the
+   * library normalises only the synthesis keys); Vs = N0(Ks_raw) gives the
+   * default mixer. */
+  FLAREPP_VARIANT_UNSHARED = 1,
+  /* Simplified FLARE++ (Appendix A.8, eq. 20):  Q = Qd =
+   * softmax_N(s Qseed Ks^T) Vs, rounded to `dtype`, then eq. 8. No fixed
+   * reference and no gate: Qf and gate must be NULL. Qseed and Ks are taken
+   * as used (the caller applies their learned-scale RMSNorms N_a; the library
+   * applies no N0 here); Vs is the unnormalised value projection. */
+  FLAREPP_VARIANT_SIMPLIFIED = 2
+} flarepp_variant_t;
+
+/*
+ * The mixer forward for one of the variants above. Arguments as for
+ * flarepp_forward, plus:
+ *   Ks     [B,H,N,D] the synthesis keys (Ks_raw of flarepp_forward for SHARED
+ *          and UNSHARED, which apply N0; used as given by SIMPLIFIED);
+ *   Vs     [B,H,N,D] the separate synthesis values (UNSHARED, SIMPLIFIED;
+ *          NULL for SHARED).
+ *   Qf, gate: required by SHARED and UNSHARED, NULL for SIMPLIFIED.
+ * Optional fp32 copies of the intermediate results as in
+ * flarepp_forward_debug (each may be NULL); SIMPLIFIED has no separate Qd
+ * (Q is Qd) and leaves Qd_out untouched. A pointer that the variant does not
+ * read but is not NULL, or one it reads that is NULL, gives
+ * FLAREPP_ERR_INVALID_ARG. Workspace comes from the per-stream cache, as for
+ * flarepp_forward. Supported sizes and dtypes as for flarepp_forward.
+ */
+flarepp_status_t flarepp_forward_variant(flarepp_variant_t variant, const void* K, const void* V,
+                                         const void* Ks, const void* Vs, const void* Qseed,
+                                         const void* Qf, const float* gate, int B, int H, int N,
+                                         int M, int D, flarepp_dtype_t dtype, void* out,
+                                         float* Qd_out, float* Q_out, float* Z_out, float* L_out,
+                                         cudaStream_t stream);
+
+/*
+ * FLARE, the fixed-query latent routing that FLARE++ builds on (Section 3.1,
+ * eq. 2-3): each head h routes through its own learned query set Q_h,
+ *   Z = softmax_N(s Q_h K^T) V,   out = softmax_M(s K Q_h^T) Z,
+ * the encode and decode steps of flarepp_forward without the synthesis.
+ *   Q      [H,M,D] of `dtype`, used as given (no normalisation);
+ *   K, V, out [B,H,N,D] as for flarepp_forward;
+ *   Z_out  [B,H,M,D] optional fp32 copy of the latents as the decode reads
+ *          them (rounded to `dtype`); L_out [B,H,M] optional fp32 encode
+ *          log-normaliser (natural log); either may be NULL.
+ * Sizes, dtypes, alignment, ownership, asynchrony and errors as for
+ * flarepp_forward; workspace from the same per-stream cache.
+ */
+flarepp_status_t flare_forward(const void* Q, const void* K, const void* V, int B, int H, int N, int M,
+                               int D, flarepp_dtype_t dtype, void* out, float* Z_out, float* L_out,
+                               cudaStream_t stream);
+
+/*
  * Waits for `stream`, then reports (and clears) any device-side error that
  * the library's kernels recorded since the last call on this device:
  * FLAREPP_ERR_TIMEOUT if a bounded wait gave up, FLAREPP_ERR_CUDA if the

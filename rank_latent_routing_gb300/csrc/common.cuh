@@ -79,6 +79,17 @@ template <typename T> __device__ __forceinline__ float round_as(float x) {
   return to_f32(from_f32<T>(x));
 }
 
+// What a split-N pass computes (FLARE++ paper):
+//  kPassEncode         SDPA(Q, K, V): the encode of eq. 8 and of FLARE's eq. 3,
+//                      and the synthesis of the simplified variant (eq. 20);
+//  kPassSynthShared    SDPA(Qseed, N0(Ks), N0(Ks)) then the gate (eq. 6-7, 19);
+//  kPassSynthSeparate  SDPA(Qseed, N0(Ks), Vs) then the gate (eq. 11).
+enum PassKind : int { kPassEncode = 0, kPassSynthShared = 1, kPassSynthSeparate = 2 };
+
+__host__ __device__ constexpr bool pass_normalises_keys(int kind) { return kind != kPassEncode; }
+__host__ __device__ constexpr bool pass_separate_values(int kind) { return kind != kPassSynthShared; }
+__host__ __device__ constexpr bool pass_gated(int kind) { return kind != kPassEncode; }
+
 // Split-N partial results of one pass (synthesis or encode), per
 // (batch*head, row tile of 128 latents, split): Z_s [128][D] fp32 normalised
 // by its own split's softmax sum, and L_s [128] its natural-log normaliser

@@ -36,12 +36,15 @@ bool stage_event(int i, cudaStream_t stream) {
 }
 
 struct Problem {
+  int variant = kVariantFlarePP;
   const void* K;
   const void* V;
   const void* Ks;
+  const void* Vs;
   const void* Qseed;
   const void* Qf;
   const float* gate;
+  const void* Q;
   int B, H, N, M, D;
   flarepp_dtype_t dtype;
   void* out;
@@ -73,13 +76,31 @@ flarepp_status_t check_sizes(int B, int H, int N, int M, int D, flarepp_dtype_t 
   return FLAREPP_OK;
 }
 
+// The inputs a variant reads: every one must be given, and the others must
+// be null (a pointer the call would ignore is more likely a mistake).
+struct Needs {
+  bool Ks, Vs, Qseed, Qf, gate, Q;
+};
+Needs needs_of(int variant) {
+  switch (variant) {
+    case kVariantFlarePP: return {true, false, true, true, true, false};
+    case kVariantUnshared: return {true, true, true, true, true, false};
+    case kVariantSimplified: return {true, true, true, false, false, false};
+    default: return {false, false, false, false, false, true};  // FLARE
+  }
+}
+
 flarepp_status_t validate(const Problem& p) {
   flarepp_status_t st = check_sizes(p.B, p.H, p.N, p.M, p.D, p.dtype);
   if (st != FLAREPP_OK) return st;
-  const void* req[] = {p.K, p.V, p.Ks, p.Qseed, p.Qf, p.gate, p.out};
-  for (const void* ptr : req)
-    if (ptr == nullptr) return FLAREPP_ERR_INVALID_ARG;
-  const void* all[] = {p.K, p.V, p.Ks, p.Qseed, p.Qf, p.gate, p.out,
+  if (p.variant < kVariantFlarePP || p.variant > kVariantFlare) return FLAREPP_ERR_INVALID_ARG;
+  const Needs n = needs_of(p.variant);
+  const std::pair<const void*, bool> opt[] = {{p.Ks, n.Ks}, {p.Vs, n.Vs}, {p.Qseed, n.Qseed},
+                                              {p.Qf, n.Qf}, {p.gate, n.gate}, {p.Q, n.Q}};
+  if (p.K == nullptr || p.V == nullptr || p.out == nullptr) return FLAREPP_ERR_INVALID_ARG;
+  for (const auto& o : opt)
+    if ((o.first != nullptr) != o.second) return FLAREPP_ERR_INVALID_ARG;
+  const void* all[] = {p.K, p.V, p.Ks, p.Vs, p.Qseed, p.Qf, p.gate, p.Q, p.out,
                        p.dbg_qd, p.dbg_q, p.dbg_z, p.dbg_l};
   for (const void* ptr : all)
     if (ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return FLAREPP_ERR_ALIGNMENT;
@@ -87,9 +108,10 @@ flarepp_status_t validate(const Problem& p) {
   const size_t tok = (size_t)p.B * p.H * p.N * p.D * es;
   const size_t lat = (size_t)p.H * p.M * p.D * es;
   const std::pair<const void*, size_t> inputs[] = {
-      {p.K, tok}, {p.V, tok}, {p.Ks, tok}, {p.Qseed, lat}, {p.Qf, lat}, {p.gate, (size_t)p.H * 4}};
+      {p.K, tok},     {p.V, tok},  {p.Ks, tok}, {p.Vs, tok}, {p.Qseed, lat},
+      {p.Qf, lat},    {p.Q, lat},  {p.gate, (size_t)p.H * 4}};
   for (const auto& in : inputs)
-    if (overlaps(p.out, tok, in.first, in.second)) return FLAREPP_ERR_INVALID_ARG;
+    if (in.first != nullptr && overlaps(p.out, tok, in.first, in.second)) return FLAREPP_ERR_INVALID_ARG;
   return FLAREPP_OK;
 }
 
@@ -163,7 +185,9 @@ flarepp_status_t launch_tc(const Problem& p, const Plan& pl, char* ws, cudaStrea
                "cudaMemsetAsync(counters)"))
     return FLAREPP_ERR_CUDA;
   DeviceProblem dp{};
-  dp.K = p.K; dp.V = p.V; dp.Ks = p.Ks; dp.Qseed = p.Qseed; dp.Qf = p.Qf; dp.gate = p.gate;
+  dp.variant = p.variant;
+  dp.K = p.K; dp.V = p.V; dp.Ks = p.Ks; dp.Vs = p.Vs; dp.Qseed = p.Qseed; dp.Qf = p.Qf; dp.gate = p.gate;
+  dp.Q = p.Q;
   dp.out = p.out;
   dp.B = p.B; dp.H = p.H; dp.N = p.N; dp.M = p.M; dp.D = p.D;
   dp.dbg_qd = p.dbg_qd; dp.dbg_q = p.dbg_q; dp.dbg_z = p.dbg_z; dp.dbg_l = p.dbg_l;
@@ -191,45 +215,63 @@ flarepp_status_t launch_typed(const Problem& p, const Plan& pl, char* ws, cudaSt
     return FLAREPP_ERR_CUDA;
 
   const dim3 grid(pl.splits, pl.tiles, pl.BH);
+  const bool flare = p.variant == kVariantFlare;
   if (!stage_event(0, stream)) return FLAREPP_ERR_CUDA;
-  simt::SplitArgs<T> sa;
-  sa.keys = static_cast<const T*>(p.Ks);
-  sa.values = static_cast<const T*>(p.Ks);
-  sa.queries = static_cast<const T*>(p.Qseed);
-  sa.qf = static_cast<const T*>(p.Qf);
-  sa.gate = p.gate;
+  simt::SplitArgs<T> sa{};
   sa.H = p.H; sa.N = p.N; sa.M = p.M;
   sa.tiles = pl.tiles; sa.splits = pl.splits; sa.split_len = pl.split_len;
   sa.part = part;
-  sa.part.counters = counters;
-  sa.out = qbuf;
-  sa.dbg_a = p.dbg_qd;
-  sa.dbg_b = p.dbg_q;
-  simt::split_kernel<T, D, true><<<grid, simt::kRows, 0, stream>>>(sa);
-  if (!cuda_ok(cudaGetLastError(), "launch synthesis")) return FLAREPP_ERR_CUDA;
+  if (!flare) {
+    // synthesis: the variant's keys, values and queries (see launch.h)
+    sa.keys = static_cast<const T*>(p.Ks);
+    sa.values = static_cast<const T*>(p.variant == kVariantFlarePP ? p.Ks : p.Vs);
+    sa.queries = static_cast<const T*>(p.Qseed);
+    sa.q_by_head = 1;
+    sa.part.counters = counters;
+    sa.out = qbuf;
+    if (p.variant == kVariantSimplified) {
+      sa.dbg_a = p.dbg_q;  // Q = Qd, as rounded
+      simt::split_kernel<T, D, kPassEncode><<<grid, simt::kRows, 0, stream>>>(sa);
+    } else {
+      sa.qf = static_cast<const T*>(p.Qf);
+      sa.gate = p.gate;
+      sa.dbg_a = p.dbg_qd;
+      sa.dbg_b = p.dbg_q;
+      if (p.variant == kVariantUnshared)
+        simt::split_kernel<T, D, kPassSynthSeparate><<<grid, simt::kRows, 0, stream>>>(sa);
+      else
+        simt::split_kernel<T, D, kPassSynthShared><<<grid, simt::kRows, 0, stream>>>(sa);
+    }
+    if (!cuda_ok(cudaGetLastError(), "launch synthesis")) return FLAREPP_ERR_CUDA;
+  }
   if (!stage_event(1, stream)) return FLAREPP_ERR_CUDA;
 
+  // routing queries: FLARE's learned per-head set, or the synthesis output
+  const T* qroute = flare ? static_cast<const T*>(p.Q) : qbuf;
   simt::SplitArgs<T> ea = sa;
   ea.keys = static_cast<const T*>(p.K);
   ea.values = static_cast<const T*>(p.V);
-  ea.queries = qbuf;
+  ea.queries = qroute;
+  ea.q_by_head = flare ? 1 : 0;
   ea.qf = nullptr;
   ea.gate = nullptr;
   ea.part.counters = counters + (size_t)pl.BH * pl.tiles;
   ea.out = zbuf;
   ea.dbg_a = p.dbg_z;
   ea.dbg_b = p.dbg_l;
-  simt::split_kernel<T, D, false><<<grid, simt::kRows, 0, stream>>>(ea);
+  simt::split_kernel<T, D, kPassEncode><<<grid, simt::kRows, 0, stream>>>(ea);
   if (!cuda_ok(cudaGetLastError(), "launch encode")) return FLAREPP_ERR_CUDA;
   if (!stage_event(2, stream)) return FLAREPP_ERR_CUDA;
 
   simt::DecodeArgs<T> da;
   da.keys = static_cast<const T*>(p.K);
-  da.q = qbuf;
+  da.q = qroute;
   da.z = zbuf;
   da.out = static_cast<T*>(p.out);
   da.N = p.N;
   da.M = p.M;
+  da.H = p.H;
+  da.q_by_head = flare ? 1 : 0;
   const size_t smem = 2 * (size_t)p.M * D * sizeof(float);
   if (!cuda_ok(cudaFuncSetAttribute(simt::decode_kernel<T, D>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
@@ -353,6 +395,38 @@ flarepp_status_t flarepp_forward_debug(const void* K, const void* V, const void*
   Problem p = flarepp::make_problem(K, V, Ks_raw, Qseed, Qf, gate, B, H, N, M, D, dtype, out);
   p.dbg_qd = Qd_out;
   p.dbg_q = Q_out;
+  p.dbg_z = Z_out;
+  p.dbg_l = L_out;
+  return flarepp::run(p, nullptr, 0, true, stream);
+}
+
+flarepp_status_t flarepp_forward_variant(flarepp_variant_t variant, const void* K, const void* V,
+                                         const void* Ks, const void* Vs, const void* Qseed,
+                                         const void* Qf, const float* gate, int B, int H, int N,
+                                         int M, int D, flarepp_dtype_t dtype, void* out,
+                                         float* Qd_out, float* Q_out, float* Z_out, float* L_out,
+                                         cudaStream_t stream) {
+  if (variant != FLAREPP_VARIANT_SHARED && variant != FLAREPP_VARIANT_UNSHARED &&
+      variant != FLAREPP_VARIANT_SIMPLIFIED)
+    return FLAREPP_ERR_INVALID_ARG;
+  Problem p = flarepp::make_problem(K, V, Ks, Qseed, Qf, gate, B, H, N, M, D, dtype, out);
+  p.variant = variant == FLAREPP_VARIANT_SHARED     ? flarepp::kVariantFlarePP
+              : variant == FLAREPP_VARIANT_UNSHARED ? flarepp::kVariantUnshared
+                                                    : flarepp::kVariantSimplified;
+  p.Vs = Vs;
+  p.dbg_qd = variant == FLAREPP_VARIANT_SIMPLIFIED ? nullptr : Qd_out;
+  p.dbg_q = Q_out;
+  p.dbg_z = Z_out;
+  p.dbg_l = L_out;
+  return flarepp::run(p, nullptr, 0, true, stream);
+}
+
+flarepp_status_t flare_forward(const void* Q, const void* K, const void* V, int B, int H, int N, int M,
+                               int D, flarepp_dtype_t dtype, void* out, float* Z_out, float* L_out,
+                               cudaStream_t stream) {
+  Problem p = flarepp::make_problem(K, V, nullptr, nullptr, nullptr, nullptr, B, H, N, M, D, dtype, out);
+  p.variant = flarepp::kVariantFlare;
+  p.Q = Q;
   p.dbg_z = Z_out;
   p.dbg_l = L_out;
   return flarepp::run(p, nullptr, 0, true, stream);

@@ -8,14 +8,26 @@
 
 namespace flarepp {
 
-// One forward call as the kernels see it. All pointers are device pointers.
+// Which mixer of the FLARE++ paper a call computes.
+enum Variant : int {
+  kVariantFlarePP = 0,     // eq. 5-8, synthesis keys shared as values (eq. 19)
+  kVariantUnshared = 1,    // eq. 11: separate synthesis values Vs
+  kVariantSimplified = 2,  // eq. 20: Q = SDPA(Qseed, Ks, Vs); no reference, no gate
+  kVariantFlare = 3,       // eq. 3: the caller's learned queries Q, no synthesis
+};
+
+// One forward call as the kernels see it. All pointers are device pointers;
+// those a variant does not use are null.
 struct DeviceProblem {
+  int variant;         // Variant
   const void* K;       // [BH][N][D]
   const void* V;       // [BH][N][D]
-  const void* Ks;      // [BH][N][D]
+  const void* Ks;      // [BH][N][D] synthesis keys (raw for the N0 variants)
+  const void* Vs;      // [BH][N][D] separate synthesis values
   const void* Qseed;   // [H][M][D]
   const void* Qf;      // [H][M][D]
   const float* gate;   // [H]
+  const void* Q;       // [H][M][D] FLARE's learned queries
   void* out;           // [BH][N][D]
   int B, H, N, M, D;
   float* dbg_qd;       // optional fp32 copies of the intermediate results

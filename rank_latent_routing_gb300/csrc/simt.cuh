@@ -18,22 +18,25 @@ constexpr int kTile = 32;    // tokens staged in shared memory per step
 template <typename T>
 struct SplitArgs {
   const T* keys;      // [BH][N][D]
-  const T* values;    // [BH][N][D]; the synthesis pass uses its keys
-  const T* queries;   // synthesis: Qseed [H][M][D]; encode: Q [BH][M][D]
-  const T* qf;        // synthesis only: Qf [H][M][D]
-  const float* gate;  // synthesis only: g [H]
+  const T* values;    // [BH][N][D]; unused when the keys serve as values
+  const T* queries;   // [H][M][D] (q_by_head) or [BH][M][D]
+  const T* qf;        // gated passes only: Qf [H][M][D]
+  const float* gate;  // gated passes only: g [H]
+  int q_by_head;
   int H, N, M, tiles, splits, split_len;
   Partials part;
-  T* out;             // synthesis: Q [BH][M][D]; encode: Z [BH][M][D]
-  float* dbg_a;       // synthesis: Qd fp32; encode: Z fp32 (as rounded); may be null
-  float* dbg_b;       // synthesis: Q fp32 (as rounded); encode: L fp32; may be null
+  T* out;             // gated: Q [BH][M][D]; encode: Z [BH][M][D]
+  float* dbg_a;       // gated: Qd fp32; encode: Z fp32 (as rounded); may be null
+  float* dbg_b;       // gated: Q fp32 (as rounded); encode: L fp32; may be null
 };
 
 // One CTA = one (split, 128-row tile of latents, batch*head). Each thread
 // owns one latent row: it scores the staged tokens, keeps a running max and
 // sum in the log2 domain and accumulates its unnormalised output row.
-template <typename T, int D, bool kSynth>
+template <typename T, int D, int kKind>
 __global__ void __launch_bounds__(kRows) split_kernel(const SplitArgs<T> a) {
+  constexpr bool kNormKeys = pass_normalises_keys(kKind);
+  constexpr bool kSepValues = pass_separate_values(kKind);
   const int s = blockIdx.x, tile = blockIdx.y, bh = blockIdx.z;
   const int h = bh % a.H;
   const int tid = threadIdx.x;
@@ -41,14 +44,14 @@ __global__ void __launch_bounds__(kRows) split_kernel(const SplitArgs<T> a) {
   const bool valid = m < a.M;
 
   __shared__ float ks[kTile][D];
-  __shared__ float vs[kSynth ? 1 : kTile][D];
+  __shared__ float vs[kSepValues ? kTile : 1][D];
   __shared__ int s_last;
 
   // queries pre-scaled by 1/sqrt(D) * log2(e): scores come out in log2 units
   float q[D];
   const float qscale = rsqrtf((float)D) * kLog2e;
   if (valid) {
-    const T* qrow = a.queries + ((size_t)(kSynth ? h : bh) * a.M + m) * D;
+    const T* qrow = a.queries + ((size_t)(a.q_by_head ? h : bh) * a.M + m) * D;
 #pragma unroll
     for (int d = 0; d < D; ++d) q[d] = to_f32(qrow[d]) * qscale;
   } else {
@@ -71,9 +74,9 @@ __global__ void __launch_bounds__(kRows) split_kernel(const SplitArgs<T> a) {
     for (int e = tid; e < kTile * D; e += kRows) {
       const bool in = e < cnt * D;
       ks[e / D][e % D] = in ? to_f32(a.keys[base + (size_t)n0 * D + e]) : 0.f;
-      if constexpr (!kSynth) vs[e / D][e % D] = in ? to_f32(a.values[base + (size_t)n0 * D + e]) : 0.f;
+      if constexpr (kSepValues) vs[e / D][e % D] = in ? to_f32(a.values[base + (size_t)n0 * D + e]) : 0.f;
     }
-    if (kSynth) {
+    if (kNormKeys) {
       // N0 of the synthesis keys (eq. 5): one thread per staged token row
       __syncthreads();
       if (tid < cnt) {
@@ -106,8 +109,8 @@ __global__ void __launch_bounds__(kRows) split_kernel(const SplitArgs<T> a) {
     for (int j = 0; j < kTile; ++j) {
       const float p = exp2f(sc[j] - mnew);
       lrun += p;
-      if constexpr (kSynth) {
-        // the synthesis pass shares its normalised keys as values (eq. 5);
+      if constexpr (!kSepValues) {
+        // the synthesis pass shares its normalised keys as values (eq. 19);
         // re-read them so the compiler does not hold the whole tile in registers
         const volatile float* kv = ks[j];
 #pragma unroll
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(kRows) split_kernel(const SplitArgs<T> a) {
 #pragma unroll
   for (int d = 0; d < D; ++d) u[d] *= invd;
   const size_t orow = (size_t)bh * a.M + m;
-  if (kSynth) {
+  if (pass_gated(kKind)) {
     // gate (eq. 7): Q = N0(Qf) + g * Qd, evaluated in fp32, then cast
     const T* qfrow = a.qf + ((size_t)h * a.M + m) * D;
     float f[D], ss = 0.f;
@@ -190,10 +193,10 @@ __global__ void __launch_bounds__(kRows) split_kernel(const SplitArgs<T> a) {
 template <typename T>
 struct DecodeArgs {
   const T* keys;  // [BH][N][D]
-  const T* q;     // [BH][M][D]
+  const T* q;     // [H][M][D] (q_by_head) or [BH][M][D]
   const T* z;     // [BH][M][D]
   T* out;         // [BH][N][D]
-  int N, M;
+  int N, M, H, q_by_head;
 };
 
 constexpr int kDecodeTokens = 128;  // tokens per CTA, one per thread
@@ -211,8 +214,9 @@ __global__ void __launch_bounds__(kDecodeTokens) decode_kernel(const DecodeArgs<
   const int tid = threadIdx.x;
   const float qscale = rsqrtf((float)D) * kLog2e;
   const size_t lbase = (size_t)bh * a.M * D;
+  const size_t qbase = (size_t)(a.q_by_head ? bh % a.H : bh) * a.M * D;
   for (int e = tid; e < a.M * D; e += kDecodeTokens) {
-    qs[e] = to_f32(a.q[lbase + e]) * qscale;
+    qs[e] = to_f32(a.q[qbase + e]) * qscale;
     zs[e] = to_f32(a.z[lbase + e]);
   }
   __syncthreads();

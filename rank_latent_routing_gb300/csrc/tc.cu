@@ -332,11 +332,12 @@ struct SplitParams {
   float* part_z;            // [BH][qtiles][splits][128][D]
   float* part_l;            // [BH][qtiles][splits][128]
   unsigned* counters;       // [BH][qgroups]
-  const __nv_bfloat16* qf;  // synthesis: [H][M][D]
-  const float* gate;        // synthesis: [H]
-  __nv_bfloat16* out;       // synthesis: Q; encode: Z ([BH][M][D])
-  float* dbg_a;             // synthesis: Qd; encode: Z (as rounded)
-  float* dbg_b;             // synthesis: Q (as rounded); encode: L
+  int q_by_head;            // latent queries [H][M][D] (1) or [BH][M][D] (0)
+  const __nv_bfloat16* qf;  // gated passes: [H][M][D]
+  const float* gate;        // gated passes: [H]
+  __nv_bfloat16* out;       // gated: Q; encode: Z ([BH][M][D])
+  float* dbg_a;             // gated: Qd; encode: Z (as rounded)
+  float* dbg_b;             // gated: Q (as rounded); encode: L
 };
 
 struct SlotPlan {
@@ -380,21 +381,25 @@ __host__ __device__ constexpr int split_scratch_bytes() {
 }
 
 // Token-tile ring depth of the split kernel: as deep as fits next to the
-// latent tiles and the ones tile (within ~200 KB).
-template <int D, bool kSynth>
+// latent tiles and the ones tile (within ~200 KB). A stage holds a key tile,
+// and a value tile unless the keys serve as values.
+template <int D, int kKind>
 __host__ __device__ constexpr int split_stages() {
-  constexpr int stage = (kSynth ? 1 : 2) * Layout<D>::kTileBytes;
+  constexpr int stage = (pass_separate_values(kKind) ? 2 : 1) * Layout<D>::kTileBytes;
   constexpr int n = (200 * 1024 - 3 * Layout<D>::kTileBytes) / stage;
   return n > kMaxStages ? kMaxStages : n;
 }
 
-template <int D, bool kSynth>
+template <int D, int kKind>
 __global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
   using L = Layout<D>;
-  constexpr int kStages = split_stages<D, kSynth>();
-  constexpr uint32_t kStageBytes = kSynth ? L::kTileBytes : 2 * L::kTileBytes;
+  constexpr bool kNormKeys = pass_normalises_keys(kKind);
+  constexpr bool kSepValues = pass_separate_values(kKind);
+  constexpr int kStages = split_stages<D, kKind>();
+  constexpr uint32_t kStageBytes = kSepValues ? 2 * L::kTileBytes : L::kTileBytes;
+  constexpr uint32_t kValueOff = kSepValues ? L::kTileBytes : 0;  // value tile within a stage
   static_assert(kStages * (int)kStageBytes >= split_scratch_bytes<D>(), "epilogue scratch exceeds the stage ring");
   extern __shared__ unsigned char smem_raw[];
   __shared__ Shared sh;
@@ -451,14 +456,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile t waits for tile t - kStages to be released, which in the lanes
     // mode needs tile t - kStages + 1 normalised, so the lag must stay below
     // kStages - 1)
-    constexpr int kLag = kSynth ? kStages / 2 : 0;
+    constexpr int kLag = kNormKeys ? kStages / 2 : 0;
     static_assert(kLag <= kStages - 2, "normaliser lag would deadlock the ring");
     int issued = 0;
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
-      if (!kSynth) prefetch_tmap(&tm_v);
-      const int qz = kSynth ? h : bh;
+      if (kSepValues) prefetch_tmap(&tm_v);
+      const int qz = p.q_by_head ? h : bh;
       mbar_arrive_expect_tx(&sh.q_full, (sp.mode == kPair ? 2 : 1) * L::kTileBytes);
       if (sp.mode == kLanes) {
         // the 64 (or fewer) latents twice: lanes 64-127 repeat lanes 0-63
@@ -479,11 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           unsigned char* dst = sStage + s * kStageBytes;
           mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
           tma_load_3d(dst, &tm_k, &sh.full[s], 0, n_begin + t * kTile, bh);
-          if (!kSynth) tma_load_3d(dst + L::kTileBytes, &tm_v, &sh.full[s], 0, n_begin + t * kTile, bh);
+          if (kSepValues) tma_load_3d(dst + kValueOff, &tm_v, &sh.full[s], 0, n_begin + t * kTile, bh);
           issued = t + 1;
         }
       }
-      if (kSynth) {
+      if (kNormKeys) {
         ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
         const int tn = t - kLag;
         if (ok && tn >= 0) ok = normalise_part<D, kStages>(sh, sStage, kStageBytes, tn, 0, lane);
@@ -506,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kLo = 0u, kAll = 0xFFFFFFFFu;
       auto stage_addr = [&](int t) { return smem_u32(sStage + (t % kStages) * kStageBytes); };
       auto ready = [&](int t) -> bool {
-        return wait_or_abort(sh, kSynth ? &sh.norm[t % kStages] : &sh.full[t % kStages], (t / kStages) & 1);
+        return wait_or_abort(sh, kNormKeys ? &sh.norm[t % kStages] : &sh.full[t % kStages], (t / kStages) & 1);
       };
       // key descriptor of the half's rows in stage 0; a stage is kStageBytes further
       const uint64_t dK0 = L::kmajor(smem_u32(sStage) + rows_off, 0);
@@ -548,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aP = tmem + k * kSlotCols + 64 * hf;
         const int t = slot_tile(sp, k, j);
         const uint32_t first = j > 0 ? 1u : 0u;
-        const uint64_t va = L::values1(stage_addr(t) + (kSynth ? 0 : L::kTileBytes), aOnes, 4 * hf);
+        const uint64_t va = L::values1(stage_addr(t) + kValueOff, aOnes, 4 * hf);
         if (sp.mode == kLanes) {
           const bool has_b = t + 1 < T;
 #pragma unroll
@@ -556,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts_masked(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kLo, kLo, kAll,
                           kAll);
           if (has_b) {
-            const uint64_t vb = L::values1(stage_addr(t + 1) + (kSynth ? 0 : L::kTileBytes), aOnes, 4 * hf);
+            const uint64_t vb = L::values1(stage_addr(t + 1) + kValueOff, aOnes, 4 * hf);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               mma_ts_masked(dO, aP + i * 8, L::adv(vb, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kAll, kAll, kLo,
@@ -589,8 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&sh.drain, 0, kWaitLimit);
     }
   } else if (warp == kWarpNorm || warp >= kWarpSoftmax + 8) {
-    // ------------------------------------------- N0 of the synthesis tiles
-    if (kSynth) {
+    // ------------------------------------------- N0 of the synthesis keys
+    if (kNormKeys) {
       const int part = warp == kWarpNorm ? 1 : warp - (kWarpSoftmax + 6);  // 1, 2, 3
       for (int t = 0; t < T; ++t)
         if (!normalise_part<D, kStages>(sh, sStage, kStageBytes, t, part, lane)) break;
@@ -771,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int d = 0; d < D; ++d) u[d] *= invd;
         const size_t orow = (size_t)bh * p.M + latent_f;
-        if (kSynth) {
+        if (pass_gated(kKind)) {
           // gate (eq. 7): Q = N0(Qf) + g * Qd in fp32, cast to bf16
           float f[D];
           load_row<D>(p.qf + ((size_t)h * p.M + latent_f) * D, f);
@@ -810,7 +815,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ----------------------------------------------------------- decode kernel
 struct DecodeParams {
-  int N, M, tiles_per_cta, stages;
+  int N, M, H, tiles_per_cta, stages;
+  int q_by_head;       // routing queries [H][M][D] (1) or [BH][M][D] (0)
   __nv_bfloat16* out;  // [BH][N][D]
 };
 
@@ -908,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_z);
       mbar_arrive_expect_tx(&sh.q_full, 2 * chunks * L::kTileBytes);
       for (int ch = 0; ch < chunks; ++ch) {
-        tma_load_3d(sQ + ch * L::kTileBytes, &tm_q, &sh.q_full, 0, ch * kTile, bh);
+        tma_load_3d(sQ + ch * L::kTileBytes, &tm_q, &sh.q_full, 0, ch * kTile, p.q_by_head ? bh % p.H : bh);
         tma_load_3d(sZ + ch * L::kTileBytes, &tm_z, &sh.q_full, 0, ch * kTile, bh);
       }
       int issued = 0;
@@ -1123,10 +1129,10 @@ bool make_map(CUtensorMap* map, const void* base, int D, int rows, int planes, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kSynth>
+template <int D, int kKind>
 size_t split_smem() {
-  const size_t stage = kSynth ? Layout<D>::kTileBytes : 2 * Layout<D>::kTileBytes;
-  return 1024 + 3 * (size_t)Layout<D>::kTileBytes + split_stages<D, kSynth>() * stage;
+  const size_t stage = (pass_separate_values(kKind) ? 2 : 1) * (size_t)Layout<D>::kTileBytes;
+  return 1024 + 3 * (size_t)Layout<D>::kTileBytes + split_stages<D, kKind>() * stage;
 }
 
 template <int D>
@@ -1135,19 +1141,45 @@ size_t decode_smem(int M) {
   return 1024 + (2 * chunks + decode_stages<D>(M) + 1) * (size_t)Layout<D>::kTileBytes + decode_xchg_bytes<D>();
 }
 
+template <int D, int kKind>
+cudaError_t launch_split(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const SplitParams& a,
+                         dim3 grid, cudaStream_t stream, const char* what, const char** failed) {
+  const size_t smem = split_smem<D, kKind>();
+  *failed = "cudaFuncSetAttribute(split_kernel)";
+  cudaError_t e = cudaFuncSetAttribute(split_kernel<D, kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  split_kernel<D, kKind><<<grid, kThreads, smem, stream>>>(mq, mk, mv, a);
+  *failed = what;
+  return cudaGetLastError();
+}
+
+// The passes of one call. The synthesis pass depends on the variant: shared
+// keys and values (eq. 19), separate values (eq. 11), the ungated synthesis of
+// the simplified variant (eq. 20, an encode-kind pass with per-head queries
+// writing Q), or none (FLARE, eq. 3, whose queries are the caller's). Encode
+// and decode are the same for all four.
 template <int D>
 cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspace& ws, cudaEvent_t* ev,
                       cudaStream_t stream, const char** failed) {
   const int BH = pr.B * pr.H;
+  const bool flare = pr.variant == kVariantFlare;
   cudaError_t e;
-  CUtensorMap m_seed, m_ks, m_qbuf, m_k, m_v, m_qdec, m_zdec;
+  CUtensorMap m_seed, m_ks, m_vs, m_qenc, m_k, m_v, m_qdec, m_zdec;
   const int qbox = pr.M <= 64 ? 64 : kTile;
+  // routing queries: the caller's per-head set (FLARE) or the synthesis output
+  const void* qsrc = flare ? pr.Q : ws.q;
+  const int qplanes = flare ? pr.H : BH;
   *failed = "cuTensorMapEncodeTiled";
-  if (!make_map(&m_seed, pr.Qseed, D, pr.M, pr.H, qbox) || !make_map(&m_ks, pr.Ks, D, pr.N, BH, kTile) ||
-      !make_map(&m_qbuf, ws.q, D, pr.M, BH, qbox) || !make_map(&m_k, pr.K, D, pr.N, BH, kTile) ||
-      !make_map(&m_v, pr.V, D, pr.N, BH, kTile) || !make_map(&m_qdec, ws.q, D, pr.M, BH, kTile) ||
+  if (!make_map(&m_qenc, qsrc, D, pr.M, qplanes, qbox) || !make_map(&m_k, pr.K, D, pr.N, BH, kTile) ||
+      !make_map(&m_v, pr.V, D, pr.N, BH, kTile) || !make_map(&m_qdec, qsrc, D, pr.M, qplanes, kTile) ||
       !make_map(&m_zdec, ws.z, D, pr.M, BH, kTile))
     return cudaErrorInvalidValue;
+  if (!flare) {
+    const void* vs = pr.variant == kVariantFlarePP ? pr.Ks : pr.Vs;
+    if (!make_map(&m_seed, pr.Qseed, D, pr.M, pr.H, qbox) || !make_map(&m_ks, pr.Ks, D, pr.N, BH, kTile) ||
+        !make_map(&m_vs, vs, D, pr.N, BH, kTile))
+      return cudaErrorInvalidValue;
+  }
 
   const dim3 grid(pl.splits, pl.qgroups, BH);
   SplitParams sp{};
@@ -1157,46 +1189,44 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
 
   if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) { *failed = "cudaEventRecord"; return e; }
   // synthesis (a1-a3)
-  {
+  if (!flare) {
     SplitParams a = sp;
     a.counters = ws.counters;
-    a.qf = static_cast<const __nv_bfloat16*>(pr.Qf);
-    a.gate = pr.gate;
+    a.q_by_head = 1;
     a.out = static_cast<__nv_bfloat16*>(ws.q);
-    a.dbg_a = pr.dbg_qd;
-    a.dbg_b = pr.dbg_q;
-    const size_t smem = split_smem<D, true>();
-    *failed = "cudaFuncSetAttribute(synthesis)";
-    if ((e = cudaFuncSetAttribute(split_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem)) != cudaSuccess)
-      return e;
-    split_kernel<D, true><<<grid, kThreads, smem, stream>>>(m_seed, m_ks, m_ks, a);
-    *failed = "launch synthesis";
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (pr.variant == kVariantSimplified) {
+      a.dbg_a = pr.dbg_q;  // Q = Qd, as rounded
+      e = launch_split<D, kPassEncode>(m_seed, m_ks, m_vs, a, grid, stream, "launch synthesis", failed);
+    } else {
+      a.qf = static_cast<const __nv_bfloat16*>(pr.Qf);
+      a.gate = pr.gate;
+      a.dbg_a = pr.dbg_qd;
+      a.dbg_b = pr.dbg_q;
+      e = pr.variant == kVariantUnshared
+              ? launch_split<D, kPassSynthSeparate>(m_seed, m_ks, m_vs, a, grid, stream, "launch synthesis", failed)
+              : launch_split<D, kPassSynthShared>(m_seed, m_ks, m_ks, a, grid, stream, "launch synthesis", failed);
+    }
+    if (e != cudaSuccess) return e;
   }
   if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) { *failed = "cudaEventRecord"; return e; }
   // encode (a4-a5)
   {
     SplitParams a = sp;
     a.counters = ws.counters + (size_t)BH * pl.qgroups;
+    a.q_by_head = flare ? 1 : 0;
     a.out = static_cast<__nv_bfloat16*>(ws.z);
     a.dbg_a = pr.dbg_z;
     a.dbg_b = pr.dbg_l;
-    const size_t smem = split_smem<D, false>();
-    *failed = "cudaFuncSetAttribute(encode)";
-    if ((e = cudaFuncSetAttribute(split_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem)) != cudaSuccess)
+    if ((e = launch_split<D, kPassEncode>(m_qenc, m_k, m_v, a, grid, stream, "launch encode", failed)) != cudaSuccess)
       return e;
-    split_kernel<D, false><<<grid, kThreads, smem, stream>>>(m_qbuf, m_k, m_v, a);
-    *failed = "launch encode";
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) { *failed = "cudaEventRecord"; return e; }
   // decode (a6)
   {
     DecodeParams d{};
-    d.N = pr.N; d.M = pr.M; d.tiles_per_cta = pl.decode_tiles_per_cta;
+    d.N = pr.N; d.M = pr.M; d.H = pr.H; d.tiles_per_cta = pl.decode_tiles_per_cta;
     d.stages = decode_stages<D>(pr.M);
+    d.q_by_head = flare ? 1 : 0;
     d.out = static_cast<__nv_bfloat16*>(pr.out);
     const size_t smem = decode_smem<D>(pr.M);
     *failed = "cudaFuncSetAttribute(decode)";

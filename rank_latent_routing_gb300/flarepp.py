@@ -7,8 +7,8 @@ used for device memory and streams. There is no CPU path: if the library is
 not built, importing this module raises.
 
 The names follow include/flarepp.h: ``forward``, ``forward_ws``,
-``forward_debug``, ``workspace_size``, ``sync_status``, ``status_string``,
-``set_splits``.
+``forward_debug``, ``forward_static``, ``forward_variant``, ``flare_forward``,
+``workspace_size``, ``sync_status``, ``status_string``, ``set_splits``.
 """
 from __future__ import annotations
 
@@ -20,6 +20,9 @@ import torch
 from .build import LIB
 
 BF16, FP32 = 0, 1
+VARIANT_SHARED, VARIANT_UNSHARED, VARIANT_SIMPLIFIED = 0, 1, 2
+_VARIANTS = {"shared": VARIANT_SHARED, "unshared": VARIANT_UNSHARED,
+             "simplified": VARIANT_SIMPLIFIED}
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "NO_MEMORY",
            5: "CUDA", 6: "TIMEOUT"}
 
@@ -48,6 +51,11 @@ def _load() -> ctypes.CDLL:
     lib.flarepp_forward_debug.restype = ctypes.c_int
     lib.flarepp_forward_static.argtypes = [vp, vp, vp, vp, vp, f32p, i, i, i, i, i, i, vp, st]
     lib.flarepp_forward_static.restype = ctypes.c_int
+    lib.flarepp_forward_variant.argtypes = [i, vp, vp, vp, vp, vp, vp, f32p, i, i, i, i, i, i,
+                                            vp, f32p, f32p, f32p, f32p, st]
+    lib.flarepp_forward_variant.restype = ctypes.c_int
+    lib.flare_forward.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp, f32p, f32p, st]
+    lib.flare_forward.restype = ctypes.c_int
     lib.flarepp_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.flarepp_workspace_size.restype = ctypes.c_size_t
     lib.flarepp_sync_status.argtypes = [st]
@@ -173,6 +181,87 @@ def forward_debug(K, V, Ks_raw, Qseed, Qf, gate, stream=None) -> dict:
                                         _ptr(res["L"]), _stream(stream))
     if rc:
         raise FlareppError(rc, "flarepp_forward_debug")
+    res["Y"] = out
+    return res
+
+
+def _check_tensors(ref, named):
+    code = _dtype_code(ref)
+    for name, t, shape, float_only in named:
+        if t is None:
+            continue
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+        if not t.is_cuda or t.device != ref.device:
+            raise ValueError(f"{name} must be a CUDA tensor on {ref.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if float_only:
+            if t.dtype != torch.float32:
+                raise TypeError(f"{name} must be float32")
+        elif _dtype_code(t) != code:
+            raise TypeError(f"{name} dtype {t.dtype} differs from K dtype {ref.dtype}")
+    return code
+
+
+def forward_variant(variant, K, V, Ks, Vs, Qseed, Qf=None, gate=None, out=None, stream=None,
+                    debug=False):
+    """One of the mixer variants of include/flarepp.h: ``variant`` is
+    "shared" (the default mixer), "unshared" (separate synthesis values Vs)
+    or "simplified" (Q = SDPA(Qseed, Ks, Vs), no reference and no gate: pass
+    Qf = gate = None). Returns ``Y`` [B,H,N,D], or with ``debug`` a dict of Y and
+    the fp32 intermediates Q, Z, L (and Qd except for "simplified"). ``out`` is
+    allocated if None."""
+    code_v = _VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    B, H, N, D = K.shape
+    M = Qseed.shape[1]
+    code = _check_tensors(K, [("V", V, (B, H, N, D), False), ("Ks", Ks, (B, H, N, D), False),
+                              ("Vs", Vs, (B, H, N, D), False), ("Qseed", Qseed, (H, M, D), False),
+                              ("Qf", Qf, (H, M, D), False), ("gate", gate, (H,), True),
+                              ("out", out, (B, H, N, D), False)])
+    if out is None:
+        out = torch.empty_like(K)
+    res = {}
+    if debug:
+        f = dict(device=K.device, dtype=torch.float32)
+        res = {"Q": torch.empty(B, H, M, D, **f), "Z": torch.empty(B, H, M, D, **f),
+               "L": torch.empty(B, H, M, **f)}
+        if code_v != VARIANT_SIMPLIFIED:
+            res["Qd"] = torch.empty(B, H, M, D, **f)
+    with torch.cuda.device(K.device):
+        rc = _lib.flarepp_forward_variant(code_v, _ptr(K), _ptr(V), _ptr(Ks), _ptr(Vs),
+                                          _ptr(Qseed), _ptr(Qf), _ptr(gate), B, H, N, M, D, code,
+                                          _ptr(out), _ptr(res.get("Qd")), _ptr(res.get("Q")),
+                                          _ptr(res.get("Z")), _ptr(res.get("L")), _stream(stream))
+    if rc:
+        raise FlareppError(rc, "flarepp_forward_variant")
+    if not debug:
+        return out
+    res["Y"] = out
+    return res
+
+
+def flare_forward(Q, K, V, out=None, stream=None, debug=False):
+    """FLARE (fixed learned queries Q [H,M,D]): Z = SDPA(Q_h, K, V),
+    Y = SDPA(K, Q_h, Z). Returns ``Y`` [B,H,N,D], or with ``debug`` a dict of Y
+    and the fp32 Z [B,H,M,D] and L [B,H,M]. ``out`` is allocated if None."""
+    B, H, N, D = K.shape
+    M = Q.shape[1]
+    code = _check_tensors(K, [("V", V, (B, H, N, D), False), ("Q", Q, (H, M, D), False),
+                              ("out", out, (B, H, N, D), False)])
+    if out is None:
+        out = torch.empty_like(K)
+    res = {}
+    if debug:
+        f = dict(device=K.device, dtype=torch.float32)
+        res = {"Z": torch.empty(B, H, M, D, **f), "L": torch.empty(B, H, M, **f)}
+    with torch.cuda.device(K.device):
+        rc = _lib.flare_forward(_ptr(Q), _ptr(K), _ptr(V), B, H, N, M, D, code, _ptr(out),
+                                _ptr(res.get("Z")), _ptr(res.get("L")), _stream(stream))
+    if rc:
+        raise FlareppError(rc, "flare_forward")
+    if not debug:
+        return out
     res["Y"] = out
     return res
 

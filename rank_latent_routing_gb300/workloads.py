@@ -341,3 +341,13 @@ def variant_inputs(wl: Workload) -> dict:
     return out
 
 
+
+
+def make_variant_head(name: str, b: int, h: int) -> dict:
+    """The (b, h) slice of ``variant_inputs`` for a named workload, drawn
+    alone: Vs [N, D] and the head's FLARE queries Qlat [M, D]."""
+    shape, dtype, structure, seed = CONFIGS[name]
+    gen = _STRUCTURES[structure]
+    ql = normal(seed, STREAM_QLAT, shape.H * shape.M * shape.D).reshape(shape.H, shape.M, shape.D)
+    return {"Vs": _round(gen(seed, STREAM_VS, shape, b, h), dtype)[1],
+            "Qlat": _round(ql, dtype)[1][h]}

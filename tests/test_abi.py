@@ -13,7 +13,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def _header_functions():
     text = open(os.path.join(ROOT, "include", "flarepp.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(flarepp_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(flare(?:pp)?_\w+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -26,14 +26,15 @@ def lib():
 def test_header_declares_the_boundary():
     names = _header_functions()
     for want in ("flarepp_forward", "flarepp_forward_ws", "flarepp_forward_debug",
-                 "flarepp_workspace_size", "flarepp_sync_status", "flarepp_status_string"):
+                 "flarepp_workspace_size", "flarepp_sync_status", "flarepp_status_string",
+                 "flarepp_forward_variant", "flare_forward"):
         assert want in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     _, path = lib
     out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
-    exported = set(re.findall(r"\bT (flarepp_\w+)", out))
+    exported = set(re.findall(r"\bT (flare(?:pp)?_\w+)", out))
     missing = [n for n in _header_functions() if n not in exported]
     assert not missing, missing
     for n in _header_functions():
@@ -79,3 +80,46 @@ def test_workspace_size_rejects_unsupported(lib):
     l.flarepp_workspace_size.restype = ctypes.c_size_t
     assert l.flarepp_workspace_size(1, 1, 64, 32, 64, 0) == 0
     assert l.flarepp_workspace_size(1, 1, 0, 32, 16, 0) == 0
+
+
+def _variant(l, variant, K, V, Ks, Vs, Qs, Qf, gate, out, B=1, H=2, N=64, M=32, D=16, dtype=0):
+    f = l.flarepp_forward_variant
+    vp = ctypes.c_void_p
+    f.argtypes = [ctypes.c_int] + [vp] * 7 + [ctypes.c_int] * 6 + [vp] * 5 + [vp]
+    f.restype = ctypes.c_int
+    return f(variant, K, V, Ks, Vs, Qs, Qf, gate, B, H, N, M, D, dtype, out, None, None, None,
+             None, None)
+
+
+def test_variant_argument_validation_without_gpu(lib):
+    """Each variant takes exactly the inputs it reads (include/flarepp.h)."""
+    l = lib[0]
+    K, V, Ks, Vs, Qs, Qf, g = [0x10000 * (i + 1) for i in range(7)]
+    out = 0x900000
+    assert _variant(l, 3, K, V, Ks, None, Qs, Qf, g, out) == 1      # unknown variant
+    assert _variant(l, 0, K, V, Ks, Vs, Qs, Qf, g, out) == 1        # shared takes no Vs
+    assert _variant(l, 1, K, V, Ks, None, Qs, Qf, g, out) == 1      # unshared needs Vs
+    assert _variant(l, 2, K, V, Ks, Vs, Qs, Qf, g, out) == 1        # simplified: no Qf, gate
+    assert _variant(l, 2, K, V, Ks, Vs, Qs, None, g, out) == 1
+    assert _variant(l, 2, K, V, None, Vs, Qs, None, None, out) == 1  # simplified needs Ks
+    assert _variant(l, 1, K, V, Ks, Vs + 8, Qs, Qf, g, out) == 3    # misaligned Vs
+    assert _variant(l, 1, K, V, Ks, Vs, Qs, Qf, g, Vs) == 1         # out aliases Vs
+    assert _variant(l, 2, K, V, Ks, Vs, Qs, None, None, out, D=64) == 2
+
+
+def test_flare_argument_validation_without_gpu(lib):
+    l = lib[0]
+    f = l.flare_forward
+    vp = ctypes.c_void_p
+    f.argtypes = [vp] * 3 + [ctypes.c_int] * 6 + [vp] * 4
+    f.restype = ctypes.c_int
+    Q, K, V, out = 0x10000, 0x20000, 0x30000, 0x900000
+
+    def call(q, k, v, o, M=32, D=16):
+        return f(q, k, v, 1, 2, 64, M, D, 0, o, None, None, None)
+
+    assert call(None, K, V, out) == 1        # null Q
+    assert call(Q, K, None, out) == 1        # null V
+    assert call(Q + 4, K, V, out) == 3       # misaligned Q
+    assert call(Q, K, V, Q) == 1             # out aliases Q
+    assert call(Q, K, V, out, M=600) == 2    # M > 512

@@ -67,3 +67,31 @@ def test_traffic_record_follows_kernel_source():
     # the committed record matches the committed kernel source
     assert t is not None and t > 16_000_000
     assert bench.measured_traffic("pde2d", "no-such-kernel") is None
+
+
+def test_variant_stage_costs():
+    """Algorithmic bytes per pass follow each variant's inputs: the synthesis
+    reads Ks_raw (D per token), Ks and Vs (2D), or nothing (FLARE)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from rank_latent_routing_gb300 import workloads
+    s = workloads.Shape(2, 3, 100, 64, 16)
+    th = 2 * 3 * 100
+    assert bench.stage_costs(s, 2)["synthesis"]["bytes"] == th * 16 * 2
+    assert bench.stage_costs(s, 2, "unshared")["synthesis"]["bytes"] == 2 * th * 16 * 2
+    assert bench.stage_costs(s, 2, "simplified")["synthesis"]["bytes"] == 2 * th * 16 * 2
+    flare = bench.stage_costs(s, 2, "flare")
+    assert flare["synthesis"] == {"bytes": 0, "flops": 0.0, "exps": 0.0}
+    assert flare["encode"]["bytes"] == 2 * th * 16 * 2
+
+
+@pytest.mark.parametrize("variant", ["flare", "simplified"])
+def test_reference_arm_variant(variant):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3", "--workload", "tiny",
+                        "--variant", variant], capture_output=True, text=True, timeout=600,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert f"{variant} mixer" in line["config"]["workload"]
