@@ -18,7 +18,9 @@ routing", arXiv 2608.11519 v2):
 * Y = SDPA(K, Q, Z), softmax over the M routes (eq. 8, Figure 1 caption).
 * the mixer variants the paper defines beside it, at the end of the module:
   FLARE (Section 3.1 eq. 3), separate synthesis values (Appendix A.1 eq. 11)
-  and simplified FLARE++ (Appendix A.8 eq. 20).
+  and simplified FLARE++ (Appendix A.8 eq. 20);
+* the token projections that produce the mixer's inputs, with their per-head
+  normalisations (Section 3.2, Appendix A.7).
 
 Readings where the paper is silent (each one is also listed in the design
 notes of the repository):
@@ -291,3 +293,48 @@ def forward_simplified(K, V, Ks, Vs, Qseed, rows: int | None = None) -> dict:
             for key, val in (("Q", q), ("Z", z), ("L", lse), ("Y", y)):
                 res[key][b, h] = val
     return res
+
+
+# ---------------------------------------------------------------- projection
+# The pointwise projections that produce the mixer's inputs (Section 3.2 and
+# Appendix A.7 Table 2: K = N_a(X W_K), V = X W_V, K~ = X W~_K, each a plain
+# linear map per token, heads split along the output channels). Readings (also
+# in the design notes):
+#
+# 9.  The output channels of one projection are ordered head-major:
+#     channel h*D + d is element d of head h (D = C / H).
+# 10. A bias, when present, is added before the normalisation.
+# 11. N_a is RMSNorm over D with a learned scale of D values shared by all
+#     heads ("D parameters when it is affine", Appendix A.7); eps = 1e-6 as N0.
+
+NORM_NONE, NORM_N0, NORM_NA = 0, 1, 2
+
+
+def project(X, W, bias, norms, scales, H: int) -> list:
+    """Fused projections of the mixer's token inputs.
+
+    X [B, N, C]; W [P*C, C] (P stacked projections, torch Linear layout
+    out x in); bias [P*C] or None; norms: P codes (NORM_NONE, NORM_N0,
+    NORM_NA); scales [P, D] (row p used when norms[p] == NORM_NA) or None.
+    Returns P float64 arrays [B, H, N, D]:
+    out_p = norm_p(X W_p^T + b_p), normalised per head over D.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    B, N, C = X.shape
+    P = len(norms)
+    D = C // H
+    y = X @ W.T  # [B, N, P*C]
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float64)
+    outs = []
+    for p in range(P):
+        part = y[:, :, p * C:(p + 1) * C].reshape(B, N, H, D).transpose(0, 2, 1, 3)
+        if norms[p] == NORM_N0:
+            part = n0(part)
+        elif norms[p] == NORM_NA:
+            part = n0(part) * np.asarray(scales[p], dtype=np.float64)
+        elif norms[p] != NORM_NONE:
+            raise ValueError(norms[p])
+        outs.append(np.ascontiguousarray(part))
+    return outs

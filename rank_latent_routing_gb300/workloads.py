@@ -48,6 +48,7 @@ _C2 = np.uint64(0x94D049BB133111EB)
 STREAM_K, STREAM_V, STREAM_KS, STREAM_QSEED, STREAM_QF, STREAM_GATE = 1, 2, 3, 4, 5, 6
 STREAM_AUX = 7  # tokens ids, points, low-rank factors and similar structure
 STREAM_VS, STREAM_QLAT = 8, 9  # separate synthesis values; FLARE's learned queries
+STREAM_X, STREAM_W, STREAM_B, STREAM_A = 10, 11, 12, 13  # projection inputs and parameters
 
 _CHUNK = 1 << 18
 
@@ -351,3 +352,44 @@ def make_variant_head(name: str, b: int, h: int) -> dict:
     ql = normal(seed, STREAM_QLAT, shape.H * shape.M * shape.D).reshape(shape.H, shape.M, shape.D)
     return {"Vs": _round(gen(seed, STREAM_VS, shape, b, h), dtype)[1],
             "Qlat": _round(ql, dtype)[1][h]}
+
+
+@dataclass
+class Projection:
+    """Inputs of the fused token projections: X [B, N, C] (C = H D), the
+    stacked weights W [P*C, C] (torch Linear layout, out x in), bias [P*C]
+    fp32, the per-head norm codes of the P outputs and the N_a scales [P, D]
+    fp32. X and W hold values exact in ``dtype``; ``bits`` has their uint16
+    patterns for bf16."""
+    B: int
+    H: int
+    N: int
+    D: int
+    dtype: str
+    X: np.ndarray
+    W: np.ndarray
+    bias: np.ndarray
+    norms: tuple
+    scales: np.ndarray
+    bits: dict = field(default_factory=dict)
+
+
+def projection_inputs(B: int, H: int, N: int, D: int, dtype: str = "bf16", seed: int = 7,
+                      norms=(2, 0, 0)) -> Projection:
+    """X ~ N(0,1) (a pre-normalised block input); W = I + dW per stacked
+    projection with dW ~ 0.02 N(0,1) clipped at two standard deviations (the
+    near-identity initialisation of the FLARE++ paper, Appendix A.5 eq. 18);
+    bias ~ 0.02 N(0,1); N_a scales ~ 1 + 0.1 N(0,1). The default norms are
+    those of the FLARE++ mixer's inputs: K = N_a(X W_K), V = X W_V and the raw
+    synthesis keys X W~_K."""
+    C = H * D
+    P = len(norms)
+    x = normal(seed, STREAM_X, B * N * C).reshape(B, N, C)
+    dw = np.clip(normal(seed, STREAM_W, P * C * C), -2.0, 2.0).reshape(P, C, C) * 0.02
+    w = (dw + np.eye(C)[None]).reshape(P * C, C)
+    bias = (normal(seed, STREAM_B, P * C) * 0.02).astype(np.float32)
+    scales = (1.0 + 0.1 * normal(seed, STREAM_A, P * D)).reshape(P, D).astype(np.float32)
+    xb, xv = _round(x, dtype)
+    wb, wv = _round(w, dtype)
+    bits = {"X": xb, "W": wb} if dtype == "bf16" else {}
+    return Projection(B, H, N, D, dtype, xv, wv, bias, tuple(int(n) for n in norms), scales, bits)
