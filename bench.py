@@ -356,6 +356,101 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+def run_project(args, rank, world, local_rank):
+    """The fused token projections (K = N_a(X W_K), V = X W_V, raw synthesis
+    keys) on the workload's B, H, N, D: X [B, N, H D] in, three [B, H, N, D]
+    out. HBM-bound at these widths; reported against the measured copy peak."""
+    import torch
+    from rank_latent_routing_gb300 import flarepp
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    s = workloads.CONFIGS[args.workload][0]
+    pr = workloads.projection_inputs(s.B, s.H, s.N, s.D, dtype="bf16", seed=3)
+    C = s.H * s.D
+    host = {"X": torch.from_numpy(np.ascontiguousarray(pr.bits["X"]).view(np.int16)).view(torch.bfloat16),
+            "W": torch.from_numpy(np.ascontiguousarray(pr.bits["W"]).view(np.int16)).view(torch.bfloat16),
+            "bias": torch.from_numpy(pr.bias), "scales": torch.from_numpy(pr.scales)}
+    dev = {k: v.to(device) for k, v in host.items()}
+    host = {k: v.pin_memory() for k, v in host.items()}
+    outs = [torch.empty(s.B, s.H, s.N, s.D, dtype=torch.bfloat16, device=device) for _ in range(3)]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        flarepp.project(dev["X"], dev["W"], s.H, pr.norms, bias=dev["bias"], scales=dev["scales"],
+                        outs=outs)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if flarepp.sync_status() != 0:
+        raise RuntimeError("device error during warm-up")
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    clk = clocks.stop(t0, t1)
+    if flarepp.sync_status() != 0:
+        raise RuntimeError("device error in timed region")
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+
+    # end to end: X from pinned host memory in, the three outputs back
+    hout = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    e2e_steps = max(5, min(args.steps, 20))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dev["X"].copy_(host["X"], non_blocking=True)
+        step()
+        for h, o in zip(hout, outs):
+            h.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    t_max, e2e_max = max_over_ranks([ms, e2e_ms], world, device)
+    if rank != 0:
+        return None
+    peaks, kind = load_peaks()
+    tokens = s.B * s.N * world
+    nbytes = s.B * s.N * C * 2 * 4 + 3 * C * C * 2  # X in, three outputs out, the weights once
+    flops = 2.0 * s.B * s.N * C * 3 * C
+    t = t_max * 1e-3
+    ach = nbytes / t / 1e9
+    return {
+        "metric": "FLARE++ token projections (K, V, synthesis keys) tokens/s", "value": round(tokens / t, 1),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_max, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, near-identity weights)",
+        "config": {"workload": f"projection of {args.workload}: B={s.B} N={s.N} C={C} (H={s.H} D={s.D}) "
+                               "-> K (N_a), V, raw synthesis keys",
+                   "l2": "512 MB flush before every timed step"},
+        "roofline": {"bound": "hbm", "kernel": "proj_kernel", "achieved": round(ach, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                     "traffic": None, "peak_source": kind,
+                     "tensor_frac": round(flops / t / 1e12 / peaks["bf16_tflops_sustained"], 4)},
+        "clocks": clk,
+        "e2e": {"value": round(tokens / (e2e_max * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(host["X"].numel() * 2),
+                "d2h_bytes_per_step": int(sum(h.numel() * 2 for h in hout)),
+                "ms_per_step": round(e2e_max, 4)},
+        "gpu_launches": args.steps,
+        "impl": "ours",
+    }
+
+
 # ------------------------------------------------------------ CPU oracle
 def _pool_init():
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -484,6 +579,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="pde2d", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--op", default="mixer", choices=["mixer", "project"],
+                    help="what to time: the mixer forward, or the fused token projections")
     ap.add_argument("--variant", default="flarepp", choices=sorted(VARIANT_INPUTS),
                     help="mixer: FLARE++ (default), separate synthesis values, simplified "
                          "FLARE++, or FLARE")
@@ -508,13 +605,13 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        line = run_ours(args, rank, world, local_rank)
+        line = (run_project if args.op == "project" else run_ours)(args, rank, world, local_rank)
     finally:
         if world > 1:
             dist.destroy_process_group()
     if line is None:
         return
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and args.op == "mixer":
         line["cpu_baseline"] = cpu_baseline(args)
     print(json.dumps(line), flush=True)
 

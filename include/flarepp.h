@@ -179,6 +179,43 @@ flarepp_status_t flare_forward(const void* Q, const void* K, const void* V, int 
                                int D, flarepp_dtype_t dtype, void* out, float* Z_out, float* L_out,
                                cudaStream_t stream);
 
+/* Per-head normalisation of a projection's output (flarepp_project). */
+typedef enum {
+  FLAREPP_NORM_NONE = 0, /* none */
+  FLAREPP_NORM_N0 = 1,   /* RMSNorm over D without scale, eps 1e-6 (N0 of Section 3.2) */
+  FLAREPP_NORM_NA = 2    /* RMSNorm over D with a learned scale of D values (N_a) */
+} flarepp_norm_t;
+
+/*
+ * The pointwise token projections that produce the mixer's inputs
+ * (Section 3.2 and Appendix A.7 Table 2 of the paper: K = N_a(X W_K),
+ * V = X W_V, the synthesis keys X W~_K; or the simplified variant's set),
+ * P of them in one pass over X:
+ *
+ *   outs[p][b, h, n, d] = norm_p( X[b, n, :] . W[p*C + h*D + d, :] + bias[p*C + h*D + d] )
+ *
+ * with C = H*D, the norm applied to each head's D values (bias first).
+ *   X      [B, N, C] of `dtype` (device), the block input after its pre-norm;
+ *   W      [P*C, C] of `dtype` (device): the P weight matrices stacked, each in
+ *          the out x in layout of a linear layer, output channel h*D + d
+ *          belonging to head h;
+ *   bias   [P*C] fp32 (device) or NULL;
+ *   norms  P codes (HOST array);
+ *   scales [P, D] fp32 (device): row p is the N_a scale of output p; NULL
+ *          exactly when no output uses FLAREPP_NORM_NA;
+ *   outs   P DEVICE pointers (HOST array), each [B, H, N, D] of `dtype`, the
+ *          layout flarepp_forward takes. They must not overlap each other or
+ *          any input.
+ * Supported: 1 <= P <= 4; D in {16, 32}; bf16 needs C in {64, 128, 256},
+ * fp32 C <= 256; B <= 65535; B*H*N*D < 2^31. The bf16 path rounds each output
+ * once (fp32 accumulation, bias and norm in fp32). Alignment, ownership,
+ * asynchrony and errors as for flarepp_forward; the call needs no workspace.
+ */
+flarepp_status_t flarepp_project(const void* X, const void* W, const float* bias, int P,
+                                 const flarepp_norm_t* norms, const float* scales, void* const* outs,
+                                 int B, int H, int N, int D, flarepp_dtype_t dtype,
+                                 cudaStream_t stream);
+
 /*
  * Waits for `stream`, then reports (and clears) any device-side error that
  * the library's kernels recorded since the last call on this device:

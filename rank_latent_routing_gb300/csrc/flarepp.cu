@@ -432,6 +432,66 @@ flarepp_status_t flare_forward(const void* Q, const void* K, const void* V, int 
   return flarepp::run(p, nullptr, 0, true, stream);
 }
 
+flarepp_status_t flarepp_project(const void* X, const void* W, const float* bias, int P,
+                                 const flarepp_norm_t* norms, const float* scales, void* const* outs,
+                                 int B, int H, int N, int D, flarepp_dtype_t dtype,
+                                 cudaStream_t stream) {
+  using flarepp::overlaps;
+  if (B <= 0 || H <= 0 || N <= 0 || D <= 0 || P < 1 || P > flarepp::kMaxProjParts)
+    return FLAREPP_ERR_INVALID_ARG;
+  if (X == nullptr || W == nullptr || norms == nullptr || outs == nullptr) return FLAREPP_ERR_INVALID_ARG;
+  if (dtype != FLAREPP_BF16 && dtype != FLAREPP_FP32) return FLAREPP_ERR_UNSUPPORTED;
+  const bool bf16 = dtype == FLAREPP_BF16;
+  if (!flarepp::proj_supported(H, D, bf16)) return FLAREPP_ERR_UNSUPPORTED;
+  if ((long long)B * H * N * D >= (1LL << 31) || B > 65535) return FLAREPP_ERR_UNSUPPORTED;
+  flarepp::ProjProblem pp{};
+  bool any_na = false;
+  for (int i = 0; i < P; ++i) {
+    if (norms[i] != FLAREPP_NORM_NONE && norms[i] != FLAREPP_NORM_N0 && norms[i] != FLAREPP_NORM_NA)
+      return FLAREPP_ERR_INVALID_ARG;
+    if (outs[i] == nullptr) return FLAREPP_ERR_INVALID_ARG;
+    any_na = any_na || norms[i] == FLAREPP_NORM_NA;
+    pp.norms[i] = static_cast<int>(norms[i]);
+    pp.outs[i] = outs[i];
+  }
+  if (any_na != (scales != nullptr)) return FLAREPP_ERR_INVALID_ARG;
+  const void* ptrs[] = {X, W, bias, scales};
+  for (const void* q : ptrs)
+    if (q != nullptr && (reinterpret_cast<uintptr_t>(q) & 15u) != 0) return FLAREPP_ERR_ALIGNMENT;
+  for (int i = 0; i < P; ++i)
+    if ((reinterpret_cast<uintptr_t>(outs[i]) & 15u) != 0) return FLAREPP_ERR_ALIGNMENT;
+  const size_t es = bf16 ? 2 : 4;
+  const size_t C = (size_t)H * D;
+  const size_t out_bytes = (size_t)B * N * C * es;
+  const std::pair<const void*, size_t> ins[] = {{X, out_bytes},
+                                                {W, (size_t)P * C * C * es},
+                                                {bias, (size_t)P * C * 4},
+                                                {scales, (size_t)P * D * 4}};
+  for (int i = 0; i < P; ++i) {
+    for (const auto& in : ins)
+      if (in.first != nullptr && overlaps(outs[i], out_bytes, in.first, in.second)) return FLAREPP_ERR_INVALID_ARG;
+    for (int k = 0; k < i; ++k)
+      if (overlaps(outs[i], out_bytes, outs[k], out_bytes)) return FLAREPP_ERR_INVALID_ARG;
+  }
+  const int sms = flarepp::device_sm_count();
+  if (sms <= 0) {
+    snprintf(flarepp::g_last_error, sizeof(flarepp::g_last_error), "no CUDA device");
+    return FLAREPP_ERR_CUDA;
+  }
+  pp.X = X;
+  pp.W = W;
+  pp.bias = bias;
+  pp.scales = scales;
+  pp.P = P;
+  pp.B = B;
+  pp.H = H;
+  pp.N = N;
+  pp.D = D;
+  const char* failed = "";
+  const cudaError_t e = flarepp::proj_forward(pp, sms, bf16, stream, &failed);
+  return flarepp::cuda_ok(e, failed) ? FLAREPP_OK : FLAREPP_ERR_CUDA;
+}
+
 flarepp_status_t flarepp_sync_status(cudaStream_t stream) {
   using flarepp::cuda_ok;
   if (!cuda_ok(cudaStreamSynchronize(stream), "cudaStreamSynchronize")) return FLAREPP_ERR_CUDA;
@@ -443,9 +503,10 @@ flarepp_status_t flarepp_sync_status(cudaStream_t stream) {
     if (!cuda_ok(cudaMemcpyToSymbol(flarepp::g_error_word, &zero, sizeof(zero)), "clear error word"))
       return FLAREPP_ERR_CUDA;
   }
-  unsigned tc_word = 0;
+  unsigned tc_word = 0, proj_word = 0;
   if (!cuda_ok(flarepp::tc_take_error_word(&tc_word), "read tensor-core error word")) return FLAREPP_ERR_CUDA;
-  word |= tc_word;
+  if (!cuda_ok(flarepp::proj_take_error_word(&proj_word), "read projection error word")) return FLAREPP_ERR_CUDA;
+  word |= tc_word | proj_word;
   if (word != 0) {
     snprintf(flarepp::g_last_error, sizeof(flarepp::g_last_error), "device error word 0x%x", word);
     return (word & flarepp::kErrTimeout) ? FLAREPP_ERR_TIMEOUT : FLAREPP_ERR_CUDA;

@@ -64,4 +64,33 @@ cudaError_t tc_forward(const DeviceProblem& p, const TcPlan& pl, const TcWorkspa
 // bounded wait timed out).
 cudaError_t tc_take_error_word(unsigned* word);
 
+// ------------------------------------------------------ token projections
+constexpr int kMaxProjParts = 4;
+enum : int { kNormNone = 0, kNormN0 = 1, kNormNa = 2 };
+
+// Kernel arguments of the projection kernels.
+struct ProjParams {
+  int N, H, P, tiles, tiles_per_b;
+  const float* bias;    // [P*C] or null
+  const float* scales;  // [P][D] (rows of N_a parts) or null
+  int norms[kMaxProjParts];
+};
+
+// One projection call: X [B][N][C] and W [P*C][C] of the model dtype, outputs
+// [B][H][N][D] of the same dtype, C = H D. Device pointers.
+struct ProjProblem {
+  const void* X;
+  const void* W;
+  const float* bias;
+  const float* scales;
+  int norms[kMaxProjParts];
+  void* outs[kMaxProjParts];
+  int P, B, H, N, D;
+};
+
+bool proj_supported(int H, int D, bool bf16);
+cudaError_t proj_forward(const ProjProblem& p, int sms, bool bf16, cudaStream_t stream, const char** failed_call);
+// Reads and clears the projection kernel's device error word.
+cudaError_t proj_take_error_word(unsigned* word);
+
 }  // namespace flarepp

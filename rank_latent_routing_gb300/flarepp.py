@@ -7,7 +7,7 @@ used for device memory and streams. There is no CPU path: if the library is
 not built, importing this module raises.
 
 The names follow include/flarepp.h: ``forward``, ``forward_ws``,
-``forward_debug``, ``forward_static``, ``forward_variant``, ``flare_forward``,
+``forward_debug``, ``forward_static``, ``forward_variant``, ``flare_forward``, ``project``,
 ``workspace_size``, ``sync_status``, ``status_string``, ``set_splits``.
 """
 from __future__ import annotations
@@ -56,6 +56,8 @@ def _load() -> ctypes.CDLL:
     lib.flarepp_forward_variant.restype = ctypes.c_int
     lib.flare_forward.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp, f32p, f32p, st]
     lib.flare_forward.restype = ctypes.c_int
+    lib.flarepp_project.argtypes = [vp, vp, f32p, i, vp, f32p, vp, i, i, i, i, i, st]
+    lib.flarepp_project.restype = ctypes.c_int
     lib.flarepp_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.flarepp_workspace_size.restype = ctypes.c_size_t
     lib.flarepp_sync_status.argtypes = [st]
@@ -264,6 +266,40 @@ def flare_forward(Q, K, V, out=None, stream=None, debug=False):
         return out
     res["Y"] = out
     return res
+
+
+NORM_NONE, NORM_N0, NORM_NA = 0, 1, 2
+_NORMS = {"none": NORM_NONE, "n0": NORM_N0, "na": NORM_NA}
+
+
+def project(X, W, H, norms, bias=None, scales=None, outs=None, stream=None):
+    """Fused token projections (include/flarepp.h ``flarepp_project``).
+
+    X [B,N,C], W [P*C, C] (stacked, out x in), ``norms`` P codes or names
+    ("none", "n0", "na"), bias [P*C] fp32 or None, scales [P,D] fp32 or None.
+    Returns the P outputs [B,H,N,D] (allocated unless ``outs`` is given)."""
+    B, N, C = X.shape
+    if C % H:
+        raise ValueError(f"C={C} is not a multiple of H={H}")
+    D = C // H
+    P = len(norms)
+    codes = [_NORMS[n] if isinstance(n, str) else int(n) for n in norms]
+    code = _check_tensors(X, [("W", W, (P * C, C), False), ("bias", bias, (P * C,), True),
+                              ("scales", scales, (P, D), True)])
+    if outs is None:
+        outs = [torch.empty(B, H, N, D, dtype=X.dtype, device=X.device) for _ in range(P)]
+    for k, o in enumerate(outs):
+        _check_tensors(X, [(f"outs[{k}]", o, (B, H, N, D), False)])
+    norm_arr = (ctypes.c_int * P)(*codes)
+    out_arr = (ctypes.c_void_p * P)(*[o.data_ptr() for o in outs])
+    with torch.cuda.device(X.device):
+        rc = _lib.flarepp_project(_ptr(X), _ptr(W), _ptr(bias), P,
+                                  ctypes.cast(norm_arr, ctypes.c_void_p), _ptr(scales),
+                                  ctypes.cast(out_arr, ctypes.c_void_p), B, H, N, D, code,
+                                  _stream(stream))
+    if rc:
+        raise FlareppError(rc, "flarepp_project")
+    return outs
 
 
 def sync_status(stream=None) -> int:

@@ -123,3 +123,32 @@ def test_flare_argument_validation_without_gpu(lib):
     assert call(Q + 4, K, V, out) == 3       # misaligned Q
     assert call(Q, K, V, Q) == 1             # out aliases Q
     assert call(Q, K, V, out, M=600) == 2    # M > 512
+
+
+def test_project_argument_validation_without_gpu(lib):
+    l = lib[0]
+    f = l.flarepp_project
+    vp = ctypes.c_void_p
+    f.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, vp] + [ctypes.c_int] * 5 + [vp]
+    f.restype = ctypes.c_int
+    X, W, bias, sc = 0x100000, 0x200000, 0x300000, 0x400000
+    outs = (ctypes.c_void_p * 3)(0x1000000, 0x2000000, 0x3000000)
+
+    def call(norms, scales=sc, P=3, H=8, D=16, dtype=0, x=X, o=outs):
+        arr = (ctypes.c_int * len(norms))(*norms)
+        return f(x, W, bias, P, ctypes.cast(arr, vp), scales, ctypes.cast(o, vp), 2, H, 64, D, dtype,
+                 None)
+
+    assert call([2, 0, 0], P=0) == 1                    # P out of range
+    assert call([2, 0, 0], P=5) == 1
+    assert call([3, 0, 0]) == 1                         # unknown norm code
+    assert call([0, 0, 0]) == 1                         # scales given but no N_a output
+    assert call([2, 0, 0], scales=None) == 1            # N_a output without scales
+    assert call([2, 0, 0], H=3) == 2                    # bf16 needs C in {64, 128, 256}
+    assert call([2, 0, 0], D=64) == 2                   # D unsupported
+    assert call([2, 0, 0], x=X + 8) == 3                # misaligned X
+    assert call([2, 0, 0], x=None) == 1                 # null X
+    same = (ctypes.c_void_p * 3)(0x1000000, 0x1000000, 0x3000000)
+    assert call([2, 0, 0], o=same) == 1                 # outputs overlap
+    onx = (ctypes.c_void_p * 3)(X, 0x2000000, 0x3000000)
+    assert call([2, 0, 0], o=onx) == 1                  # output aliases X
