@@ -20,8 +20,8 @@
 //  * one thread issues the tcgen05 MMAs (M = 128 tokens, N = 128 channels,
 //    K = 16) into four 128-column TMEM accumulators, so the tensor core fills
 //    the next chunks while the epilogue drains one;
-//  * eight epilogue warps (two per TMEM lane quarter, one per 64-channel half)
-//    add the bias, normalise each head's D values, round to bf16, write the
+//  * epilogue warps in groups of four (one per TMEM lane quarter), each group
+//    taking 32 or 64 channels of every chunk, add the bias, normalise each head's D values, round to bf16, write the
 //    head tiles [128 tokens, D] into shared memory in the swizzled layout of
 //    the mixer's token tiles, and TMA-store them straight into [B, H, N, D];
 //    rows past N are clipped by the store.
@@ -47,7 +47,6 @@ using namespace sm100;
 __device__ unsigned g_proj_error = 0u;
 
 constexpr int kTok = 128;        // tokens per tile (MMA M, TMEM lanes)
-constexpr int kThreads = 384;    // warps 0-3 producers / MMA, 4-11 epilogue
 constexpr int kWarpX = 0;        // lane 0: TMA loads of X tiles
 constexpr int kWarpMma = 1;      // lane 0: MMA issue; the warp owns TMEM
 constexpr int kWarpW = 2;        // lane 0: TMA loads of weight stages
@@ -59,25 +58,31 @@ template <int D, int C>
 struct Cfg {
   static constexpr int kKc = C / 64;                    // 64-element input chunks (128-byte rows)
   static constexpr int kChunk = C >= 128 ? 128 : 64;    // output channels per accumulator
-  static constexpr int kHalf = kChunk / 2;              // channels per epilogue group
-  static constexpr int kHeadsHalf = kHalf / D;          // whole heads per group
+  // channels per epilogue group (4 warps): at C = 256 two groups of 64, so
+  // that fewer epilogue warps compete for issue slots with the MMA thread,
+  // whose issue rate bounds that width; otherwise groups of 32
+  static constexpr int kGroupCh = C == 256 ? 64 : 32;
+  static constexpr int kGroups = kChunk / kGroupCh;     // epilogue groups (4 warps each)
+  static constexpr int kHeadsGroup = kGroupCh / D;      // whole heads per group
+  static constexpr int kThreads = 32 * kWarpEpi + 128 * kGroups;
   static constexpr uint32_t kXChunkBytes = kTok * 128;  // [128 tokens, 64 inputs]
   static constexpr uint32_t kXBytes = kKc * kXChunkBytes;
   static constexpr uint32_t kWStageBytes = kChunk * 128;
-  static constexpr int kWStages = C == 256 ? 3 : 4;
+  static constexpr int kWStages = C == 256 ? 3 : 7;  // as deep as shared memory allows
   static constexpr uint32_t kHeadTileBytes = kTok * D * 2;
-  static constexpr uint32_t kStageOutBytes = kHeadsHalf * kHeadTileBytes;
+  static constexpr uint32_t kStageOutBytes = kHeadsGroup * kHeadTileBytes;
+  static constexpr uint32_t kParamFloats = kMaxProjParts * (C + D);  // bias and N_a scales
   static constexpr uint32_t kTmemCols = kAccBufs * kChunk;
   static constexpr size_t kSmem = 1024 + 2 * (size_t)kXBytes + kWStages * (size_t)kWStageBytes +
-                                  2 * (size_t)kStageOutBytes;
+                                  kGroups * (size_t)kStageOutBytes + kParamFloats * 4;
   static_assert(C % 64 == 0 && C <= 256, "C = H D must be 64, 128 or 256");
-  static_assert(kHalf % D == 0, "an epilogue group holds whole heads");
+  static_assert(kGroupCh % D == 0, "an epilogue group holds whole heads");
   static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 struct Bars {
   uint64_t x_full[2], x_empty[2];
-  uint64_t w_full[4], w_empty[4];
+  uint64_t w_full[8], w_empty[8];
   uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   uint64_t drain;
   uint32_t tmem_base;
@@ -113,7 +118,7 @@ struct OutMaps {
 };
 
 template <int D, int C>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, C>::kThreads, 1)
     proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ OutMaps tm_out, const ProjParams p) {
   using G = Cfg<D, C>;
@@ -123,7 +128,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                          ~static_cast<uintptr_t>(1023));
   unsigned char* sX = smem;                                    // [2][kKc][128 x 128 B]
   unsigned char* sW = sX + 2 * G::kXBytes;                     // [kWStages][kChunk x 128 B]
-  unsigned char* sOut = sW + G::kWStages * G::kWStageBytes;    // [2 groups][heads][128 x D]
+  unsigned char* sOut = sW + G::kWStages * G::kWStageBytes;    // [groups][heads][128 x D]
+  float* sBias = reinterpret_cast<float*>(sOut + G::kGroups * G::kStageOutBytes);  // [P*C]
+  float* sScale = sBias + kMaxProjParts * C;                                       // [P][D]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles =
       p.tiles > (int)blockIdx.x ? (p.tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
@@ -140,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kAccBufs; ++i) {
       mbar_init(&sh.acc_full[i], 1);
-      mbar_init(&sh.acc_empty[i], 8);  // one arrival per epilogue warp
+      mbar_init(&sh.acc_empty[i], 4 * G::kGroups);  // one arrival per epilogue warp
     }
     mbar_init(&sh.drain, 1);
     sh.abort = 0;
@@ -243,12 +250,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kWarpEpi) {
     // --------------------------------------------------------- epilogue
-    const int g = (warp - kWarpEpi) >> 2;  // channel half of every chunk
+    const int g = (warp - kWarpEpi) >> 2;  // 32-channel group of every chunk
     const int qd = warp & 3;               // TMEM lane quarter
     const int row = 32 * qd + lane;        // token within the tile
     const bool leader = warp == kWarpEpi + 4 * g && lane == 0;  // issues the group's stores
     unsigned char* stage = sOut + g * G::kStageOutBytes;
     const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+    // the bias and the N_a scales, once per CTA (0 and 1 where absent)
+    const int etid = threadIdx.x - 32 * kWarpEpi;
+    for (int e = etid; e < p.P * C; e += 128 * G::kGroups) sBias[e] = p.bias != nullptr ? p.bias[e] : 0.f;
+    for (int e = etid; e < p.P * D; e += 128 * G::kGroups) sScale[e] = p.scales != nullptr ? p.scales[e] : 1.f;
+    named_bar_sync(15, 128 * G::kGroups);
     int cit = 0;
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
@@ -258,13 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a = cit % kAccBufs;
         ok = ok && wait_or_abort(sh, &sh.acc_full[a], (cit / kAccBufs) & 1);
         tc_fence_after();
-        uint32_t v[G::kHalf];
+        uint32_t v[G::kGroupCh];
         if (ok) {
-          const uint32_t src = tmem + lane_base + a * G::kChunk + g * G::kHalf;
-          if constexpr (G::kHalf == 64) {
-            tmem_ld64(src, *reinterpret_cast<uint32_t(*)[64]>(v));
+          const uint32_t src = tmem + lane_base + a * G::kChunk + g * G::kGroupCh;
+          if constexpr (G::kGroupCh == 64) {
+            tmem_ld64(src, v);
           } else {
-            tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(v));
+            tmem_ld32(src, v);
           }
           tmem_wait_ld_regs(v);
         }
@@ -272,28 +284,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the group's staging buffer is free once its previous stores have read it
         if (leader) bulk_wait_group_read<0>();
         named_bar_sync(1 + g, 128);
-        const int o0 = c * G::kChunk + g * G::kHalf;  // first output channel of the group
+        const int o0 = c * G::kChunk + g * G::kGroupCh;  // first output channel of the group
         const int part = o0 / C;
         const int h0 = (o0 % C) / D;
         if (ok) {
-          const int norm = p.norms[part];
+          // select by comparison: a dynamic index into the parameter array
+          // would copy it to local memory
+          int norm = p.norms[0];
 #pragma unroll
-          for (int hh = 0; hh < G::kHeadsHalf; ++hh) {
+          for (int q = 1; q < kMaxProjParts; ++q)
+            if (part == q) norm = p.norms[q];
+#pragma unroll
+          for (int hh = 0; hh < G::kHeadsGroup; ++hh) {
             float x[D];
+            const float4* bq = reinterpret_cast<const float4*>(sBias + o0 + hh * D);
 #pragma unroll
-            for (int d = 0; d < D; ++d) {
-              x[d] = __uint_as_float(v[hh * D + d]);
-              if (p.bias != nullptr) x[d] += __ldg(p.bias + o0 + hh * D + d);
+            for (int d = 0; d < D; d += 4) {
+              const float4 bb = bq[d / 4];
+              x[d] = __uint_as_float(v[hh * D + d]) + bb.x;
+              x[d + 1] = __uint_as_float(v[hh * D + d + 1]) + bb.y;
+              x[d + 2] = __uint_as_float(v[hh * D + d + 2]) + bb.z;
+              x[d + 3] = __uint_as_float(v[hh * D + d + 3]) + bb.w;
             }
             if (norm != kNormNone) {
               float ss = 0.f;
 #pragma unroll
               for (int d = 0; d < D; ++d) ss = fmaf(x[d], x[d], ss);
               const float r = rsqrtf(ss / (float)D + kEps);
+              if (norm == kNormNa) {
+                const float4* sq = reinterpret_cast<const float4*>(sScale + part * D);
 #pragma unroll
-              for (int d = 0; d < D; ++d) {
-                x[d] *= r;
-                if (norm == kNormNa) x[d] *= __ldg(p.scales + part * D + d);
+                for (int d = 0; d < D; d += 4) {
+                  const float4 a4 = sq[d / 4];
+                  x[d] *= r * a4.x;
+                  x[d + 1] *= r * a4.y;
+                  x[d + 2] *= r * a4.z;
+                  x[d + 3] *= r * a4.w;
+                }
+              } else {
+#pragma unroll
+                for (int d = 0; d < D; ++d) x[d] *= r;
               }
             }
             unsigned char* tile = stage + hh * G::kHeadTileBytes;
@@ -311,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader && ok) {
           const CUtensorMap* m = &tm_out.m[part];
 #pragma unroll
-          for (int hh = 0; hh < G::kHeadsHalf; ++hh)
+          for (int hh = 0; hh < G::kHeadsGroup; ++hh)
             tma_store_3d(m, stage + hh * G::kHeadTileBytes, 0, j * kTok, b * p.H + h0 + hh);
           bulk_commit_group();
         }
@@ -400,7 +430,7 @@ cudaError_t launch_tc(const ProjProblem& pp, const ProjParams& prm, int sms, cud
                                        (int)G::kSmem);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(prm.tiles, sms));
-  proj_kernel<D, C><<<grid, kThreads, G::kSmem, stream>>>(mx, mw, mo, prm);
+  proj_kernel<D, C><<<grid, G::kThreads, G::kSmem, stream>>>(mx, mw, mo, prm);
   *failed = "launch proj_kernel";
   return cudaGetLastError();
 }
