@@ -305,7 +305,8 @@ def forward_simplified(K, V, Ks, Vs, Qseed, rows: int | None = None) -> dict:
 #     channel h*D + d is element d of head h (D = C / H).
 # 10. A bias, when present, is added before the normalisation.
 # 11. N_a is RMSNorm over D with a learned scale of D values shared by all
-#     heads ("D parameters when it is affine", Appendix A.7); eps = 1e-6 as N0.
+#     heads (Appendix A.7 counts D parameters for an affine per-head norm);
+#     eps = 1e-6 as N0.
 
 NORM_NONE, NORM_N0, NORM_NA = 0, 1, 2
 
