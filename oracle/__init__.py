@@ -8,10 +8,10 @@ from .flarepp_oracle import (EPS, decode, encode, encode_partial, flare_forward,
                              forward_unshared, logsumexp_rows, lse_merge, n0, routing_queries,
                              sdpa, softmax_rows, synthesis, synthesis_simplified,
                              synthesis_unshared, w_eff, NORM_NONE, NORM_N0, NORM_NA,
-                             project)
+                             project, sdpa_backward, n0_backward, backward_head, backward)
 
 __all__ = ["EPS", "decode", "encode", "encode_partial", "flare_forward", "flare_forward_head",
            "forward", "forward_head", "forward_simplified", "forward_unshared", "logsumexp_rows",
            "lse_merge", "n0", "routing_queries", "sdpa", "softmax_rows", "synthesis",
            "synthesis_simplified", "synthesis_unshared", "w_eff", "NORM_NONE", "NORM_N0",
-           "NORM_NA", "project"]
+           "NORM_NA", "project", "sdpa_backward", "n0_backward", "backward_head", "backward"]

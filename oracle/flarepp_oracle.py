@@ -20,7 +20,9 @@ routing", arXiv 2608.11519 v2):
   FLARE (Section 3.1 eq. 3), separate synthesis values (Appendix A.1 eq. 11)
   and simplified FLARE++ (Appendix A.8 eq. 20);
 * the token projections that produce the mixer's inputs, with their per-head
-  normalisations (Section 3.2, Appendix A.7).
+  normalisations (Section 3.2, Appendix A.7);
+* the mixer's backward pass (Appendix B.5 eq. 46-49 for each attention call,
+  the chain rule through the gate and N0).
 
 Readings where the paper is silent (each one is also listed in the design
 notes of the repository):
@@ -339,3 +341,83 @@ def project(X, W, bias, norms, scales, H: int) -> list:
             raise ValueError(norms[p])
         outs.append(np.ascontiguousarray(part))
     return outs
+
+
+# ------------------------------------------------------------------ backward
+# Reverse mode of the mixer (the training direction). For each attention call
+# out = softmax(s q k^T) v the local backward of Appendix B.5 eq. 46-49 is
+# used with a single shard (the merged L, so P = exp(S - L)) and no cotangent
+# on L (the mixer's output does not depend on L):
+#   dv = P^T dout,  c = <dout, out>_D per row,  dS = P o (dout v^T - c),
+#   dk = s dS^T q,  dq = s dS k.
+# The decode is the same call with the softmax over the M routes (queries K,
+# keys Q, values Z). The gate and N0 follow by the chain rule; the per-head
+# parameters (Qseed, Qf, g) collect their gradient over the batch.
+# Reading (also in the design notes):
+# 12. Gradients flow through Q as the forward computed it, unrounded; the
+#     routing queries, seeds and fixed queries are treated as exact.
+
+
+def sdpa_backward(q, k, v, dout):
+    """Gradients (dq, dk, dv) of out = SDPA(q, k, v) for the cotangent dout
+    (Appendix B.5 eq. 46-49 with one shard and zero cotangent on L)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    dout = np.asarray(dout, dtype=np.float64)
+    s = 1.0 / math.sqrt(q.shape[1])
+    scores = s * (q @ k.T)
+    lse = logsumexp_rows(scores)
+    p = np.exp(scores - lse[:, None])
+    out = p @ v
+    dv = p.T @ dout
+    c = np.sum(dout * out, axis=1)
+    ds = p * (dout @ v.T - c[:, None])
+    return s * (ds @ k), s * (ds.T @ q), dv
+
+
+def n0_backward(x, dy, eps: float = EPS):
+    """Gradient of y = N0(x) row-wise: dx = r (dy - y <dy, y> / D), r = (ms + eps)^-1/2."""
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    y = x * r
+    return r * (dy - y * np.mean(dy * y, axis=-1, keepdims=True))
+
+
+def backward_head(k, v, ks_raw, qseed_h, qf_h, g, dy) -> dict:
+    """Gradients of the mixer for one (batch, head) given dY [N, D]:
+    dK, dV, dKs_raw [N, D], dQseed, dQf [M, D] and dgate (a float)."""
+    kt = n0(ks_raw)
+    qd = sdpa(qseed_h, kt, kt)
+    q = routing_queries(qf_h, qd, g)
+    z = sdpa(q, k, v)
+    dk_dec, dq_dec, dz = sdpa_backward(k, q, z, dy)   # decode: queries K, keys Q, values Z
+    dq_enc, dk_enc, dv = sdpa_backward(q, k, v, dz)   # encode
+    dq = dq_dec + dq_enc
+    dqd = float(g) * dq
+    dgate = float(np.sum(dq * qd))
+    dqf = n0_backward(qf_h, dq)
+    dqseed, dkt_keys, dkt_vals = sdpa_backward(qseed_h, kt, kt, dqd)
+    dks = n0_backward(ks_raw, dkt_keys + dkt_vals)
+    return {"dK": dk_dec + dk_enc, "dV": dv, "dKs_raw": dks, "dQseed": dqseed, "dQf": dqf,
+            "dgate": dgate}
+
+
+def backward(K, V, Ks_raw, Qseed, Qf, gate, dY) -> dict:
+    """Gradients over all batches and heads: dK, dV, dKs_raw [B,H,N,D];
+    dQseed, dQf [H,M,D] and dgate [H], summed over the batch."""
+    B, H, N, D = K.shape
+    M = Qseed.shape[1]
+    res = {"dK": np.empty((B, H, N, D)), "dV": np.empty((B, H, N, D)),
+           "dKs_raw": np.empty((B, H, N, D)), "dQseed": np.zeros((H, M, D)),
+           "dQf": np.zeros((H, M, D)), "dgate": np.zeros(H)}
+    for b in range(B):
+        for h in range(H):
+            r = backward_head(K[b, h], V[b, h], Ks_raw[b, h], Qseed[h], Qf[h], gate[h], dY[b, h])
+            for key in ("dK", "dV", "dKs_raw"):
+                res[key][b, h] = r[key]
+            res["dQseed"][h] += r["dQseed"]
+            res["dQf"][h] += r["dQf"]
+            res["dgate"][h] += r["dgate"]
+    return res
