@@ -217,6 +217,29 @@ flarepp_status_t flarepp_project(const void* X, const void* W, const float* bias
                                  cudaStream_t stream);
 
 /*
+ * Backward pass of the mixer (flarepp_forward): given the cotangent dY of the
+ * output, the gradients of every input,
+ *   dK, dV, dKs_raw [B,H,N,D], dQseed, dQf [H,M,D] (summed over the batch),
+ *   dgate [H] (summed over the batch and the routes),
+ * all fp32 DEVICE arrays whatever `dtype` is. The inputs are those of
+ * flarepp_forward plus dY [B,H,N,D] of `dtype`. Each attention call is
+ * differentiated with the local backward of Appendix B.5 (eq. 46-49: the
+ * merged log-normaliser recovers the probabilities, c = <dOut, Out> per row,
+ * no cotangent on L); the gate (eq. 7) and both N0s follow by the chain rule.
+ * The call recomputes the forward's synthesis and encode (nothing has to be
+ * kept from the forward) and runs in fp32 arithmetic on the CUDA cores; for
+ * bf16 it uses Q and Z rounded to bf16, as the forward does. Results are
+ * bitwise repeatable (every reduction has a fixed order). Workspace comes
+ * from the per-stream cache of flarepp_forward. Sizes, alignment, ownership,
+ * asynchrony and errors as for flarepp_forward; the outputs must not overlap
+ * each other or any input.
+ */
+flarepp_status_t flarepp_backward(const void* K, const void* V, const void* Ks_raw, const void* Qseed,
+                                  const void* Qf, const float* gate, const void* dY, int B, int H, int N,
+                                  int M, int D, flarepp_dtype_t dtype, float* dK, float* dV, float* dKs_raw,
+                                  float* dQseed, float* dQf, float* dgate, cudaStream_t stream);
+
+/*
  * Waits for `stream`, then reports (and clears) any device-side error that
  * the library's kernels recorded since the last call on this device:
  * FLAREPP_ERR_TIMEOUT if a bounded wait gave up, FLAREPP_ERR_CUDA if the

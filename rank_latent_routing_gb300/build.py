@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libflarepp.so")
-SOURCES = ["flarepp.cu", "tc.cu", "proj.cu", "flarepp_static.cu"]
+SOURCES = ["flarepp.cu", "tc.cu", "proj.cu", "backward.cu", "flarepp_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

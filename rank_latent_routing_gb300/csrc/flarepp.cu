@@ -492,6 +492,50 @@ flarepp_status_t flarepp_project(const void* X, const void* W, const float* bias
   return flarepp::cuda_ok(e, failed) ? FLAREPP_OK : FLAREPP_ERR_CUDA;
 }
 
+flarepp_status_t flarepp_backward(const void* K, const void* V, const void* Ks_raw, const void* Qseed,
+                                  const void* Qf, const float* gate, const void* dY, int B, int H, int N,
+                                  int M, int D, flarepp_dtype_t dtype, float* dK, float* dV, float* dKs_raw,
+                                  float* dQseed, float* dQf, float* dgate, cudaStream_t stream) {
+  using flarepp::overlaps;
+  flarepp_status_t st = flarepp::check_sizes(B, H, N, M, D, dtype);
+  if (st != FLAREPP_OK) return st;
+  const void* req[] = {K, V, Ks_raw, Qseed, Qf, gate, dY, dK, dV, dKs_raw, dQseed, dQf, dgate};
+  for (const void* q : req) {
+    if (q == nullptr) return FLAREPP_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0) return FLAREPP_ERR_ALIGNMENT;
+  }
+  const size_t es = dtype == FLAREPP_BF16 ? 2 : 4;
+  const size_t tok = (size_t)B * H * N * D, lat = (size_t)H * M * D;
+  const std::pair<const void*, size_t> ins[] = {{K, tok * es},     {V, tok * es},   {Ks_raw, tok * es},
+                                                {Qseed, lat * es}, {Qf, lat * es},  {gate, (size_t)H * 4},
+                                                {dY, tok * es}};
+  const std::pair<const void*, size_t> outs[] = {{dK, tok * 4},     {dV, tok * 4},  {dKs_raw, tok * 4},
+                                                 {dQseed, lat * 4}, {dQf, lat * 4}, {dgate, (size_t)H * 4}};
+  for (size_t i = 0; i < 6; ++i) {
+    for (const auto& in : ins)
+      if (overlaps(outs[i].first, outs[i].second, in.first, in.second)) return FLAREPP_ERR_INVALID_ARG;
+    for (size_t k = 0; k < i; ++k)
+      if (overlaps(outs[i].first, outs[i].second, outs[k].first, outs[k].second)) return FLAREPP_ERR_INVALID_ARG;
+  }
+  const int sms = flarepp::device_sm_count();
+  if (sms <= 0) {
+    snprintf(flarepp::g_last_error, sizeof(flarepp::g_last_error), "no CUDA device");
+    return FLAREPP_ERR_CUDA;
+  }
+  const bool bf16 = dtype == FLAREPP_BF16;
+  void* ws = nullptr;
+  st = flarepp::cached_workspace(flarepp::backward_workspace_bytes(B, H, N, M, D, bf16, sms), stream, &ws);
+  if (st != FLAREPP_OK) return st;
+  flarepp::BwdProblem p{};
+  p.K = K; p.V = V; p.Ks = Ks_raw; p.Qseed = Qseed; p.Qf = Qf; p.gate = gate; p.dY = dY;
+  p.B = B; p.H = H; p.N = N; p.M = M; p.D = D; p.bf16 = bf16;
+  p.dK = dK; p.dV = dV; p.dKs = dKs_raw; p.dQseed = dQseed; p.dQf = dQf; p.dgate = dgate;
+  const char* failed = "";
+  const cudaError_t e = flarepp::backward_run(p, ws, flarepp::backward_workspace_bytes(B, H, N, M, D, bf16, sms),
+                                              sms, stream, &failed);
+  return flarepp::cuda_ok(e, failed) ? FLAREPP_OK : FLAREPP_ERR_CUDA;
+}
+
 flarepp_status_t flarepp_sync_status(cudaStream_t stream) {
   using flarepp::cuda_ok;
   if (!cuda_ok(cudaStreamSynchronize(stream), "cudaStreamSynchronize")) return FLAREPP_ERR_CUDA;

@@ -93,4 +93,29 @@ cudaError_t proj_forward(const ProjProblem& p, int sms, bool bf16, cudaStream_t 
 // Reads and clears the projection kernel's device error word.
 cudaError_t proj_take_error_word(unsigned* word);
 
+// ------------------------------------------------------------- backward
+// One backward call: the forward's inputs and dY of the model dtype, the
+// gradients in fp32. Device pointers.
+struct BwdProblem {
+  const void* K;
+  const void* V;
+  const void* Ks;
+  const void* Qseed;
+  const void* Qf;
+  const float* gate;
+  const void* dY;
+  int B, H, N, M, D;
+  bool bf16;
+  float* dK;      // [B][H][N][D]
+  float* dV;      // [B][H][N][D]
+  float* dKs;     // [B][H][N][D]
+  float* dQseed;  // [H][M][D]
+  float* dQf;     // [H][M][D]
+  float* dgate;   // [H]
+};
+
+size_t backward_workspace_bytes(int B, int H, int N, int M, int D, bool bf16, int sms);
+cudaError_t backward_run(const BwdProblem& p, void* ws, size_t ws_bytes, int sms, cudaStream_t stream,
+                         const char** failed_call);
+
 }  // namespace flarepp

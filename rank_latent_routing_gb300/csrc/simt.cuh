@@ -28,6 +28,7 @@ struct SplitArgs {
   T* out;             // gated: Q [BH][M][D]; encode: Z [BH][M][D]
   float* dbg_a;       // gated: Qd fp32; encode: Z fp32 (as rounded); may be null
   float* dbg_b;       // gated: Q fp32 (as rounded); encode: L fp32; may be null
+  float* dbg_c;       // gated: L of the synthesis softmax (natural log); may be null
 };
 
 // One CTA = one (split, 128-row tile of latents, batch*head). Each thread
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kRows) split_kernel(const SplitArgs<T> a) {
 #pragma unroll
     for (int d = 0; d < D; ++d) qo[d] = fmaf(g, u[d], f[d] * r);
     if (a.dbg_a) store_row<D>(a.dbg_a + orow * D, u);
+    if (a.dbg_c) a.dbg_c[orow] = lmax + logf(dsum);
 #pragma unroll
     for (int d = 0; d < D; ++d) {
       a.out[orow * D + d] = from_f32<T>(qo[d]);

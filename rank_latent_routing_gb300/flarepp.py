@@ -8,6 +8,7 @@ not built, importing this module raises.
 
 The names follow include/flarepp.h: ``forward``, ``forward_ws``,
 ``forward_debug``, ``forward_static``, ``forward_variant``, ``flare_forward``, ``project``,
+``backward``,
 ``workspace_size``, ``sync_status``, ``status_string``, ``set_splits``.
 """
 from __future__ import annotations
@@ -58,6 +59,9 @@ def _load() -> ctypes.CDLL:
     lib.flare_forward.restype = ctypes.c_int
     lib.flarepp_project.argtypes = [vp, vp, f32p, i, vp, f32p, vp, i, i, i, i, i, st]
     lib.flarepp_project.restype = ctypes.c_int
+    lib.flarepp_backward.argtypes = [vp, vp, vp, vp, vp, f32p, vp, i, i, i, i, i, i,
+                                     f32p, f32p, f32p, f32p, f32p, f32p, st]
+    lib.flarepp_backward.restype = ctypes.c_int
     lib.flarepp_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.flarepp_workspace_size.restype = ctypes.c_size_t
     lib.flarepp_sync_status.argtypes = [st]
@@ -266,6 +270,26 @@ def flare_forward(Q, K, V, out=None, stream=None, debug=False):
         return out
     res["Y"] = out
     return res
+
+
+def backward(K, V, Ks_raw, Qseed, Qf, gate, dY, stream=None) -> dict:
+    """Gradients of the mixer for the output cotangent dY [B,H,N,D]: a dict
+    of fp32 tensors dK, dV, dKs_raw [B,H,N,D], dQseed, dQf [H,M,D] and dgate
+    [H] (include/flarepp.h ``flarepp_backward``)."""
+    B, H, N, M, D, code = _check(K, V, Ks_raw, Qseed, Qf, gate)
+    _check_tensors(K, [("dY", dY, (B, H, N, D), False)])
+    f = dict(device=K.device, dtype=torch.float32)
+    g = {"dK": torch.empty(B, H, N, D, **f), "dV": torch.empty(B, H, N, D, **f),
+         "dKs_raw": torch.empty(B, H, N, D, **f), "dQseed": torch.empty(H, M, D, **f),
+         "dQf": torch.empty(H, M, D, **f), "dgate": torch.empty(H, **f)}
+    with torch.cuda.device(K.device):
+        rc = _lib.flarepp_backward(_ptr(K), _ptr(V), _ptr(Ks_raw), _ptr(Qseed), _ptr(Qf),
+                                   _ptr(gate), _ptr(dY), B, H, N, M, D, code, _ptr(g["dK"]),
+                                   _ptr(g["dV"]), _ptr(g["dKs_raw"]), _ptr(g["dQseed"]),
+                                   _ptr(g["dQf"]), _ptr(g["dgate"]), _stream(stream))
+    if rc:
+        raise FlareppError(rc, "flarepp_backward")
+    return g
 
 
 NORM_NONE, NORM_N0, NORM_NA = 0, 1, 2

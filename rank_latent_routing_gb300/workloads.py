@@ -49,6 +49,7 @@ STREAM_K, STREAM_V, STREAM_KS, STREAM_QSEED, STREAM_QF, STREAM_GATE = 1, 2, 3, 4
 STREAM_AUX = 7  # tokens ids, points, low-rank factors and similar structure
 STREAM_VS, STREAM_QLAT = 8, 9  # separate synthesis values; FLARE's learned queries
 STREAM_X, STREAM_W, STREAM_B, STREAM_A = 10, 11, 12, 13  # projection inputs and parameters
+STREAM_DY = 14  # output cotangents of the backward pass
 
 _CHUNK = 1 << 18
 
@@ -393,3 +394,15 @@ def projection_inputs(B: int, H: int, N: int, D: int, dtype: str = "bf16", seed:
     wb, wv = _round(w, dtype)
     bits = {"X": xb, "W": wb} if dtype == "bf16" else {}
     return Projection(B, H, N, D, dtype, xv, wv, bias, tuple(int(n) for n in norms), scales, bits)
+
+
+def cotangent(wl: Workload, seed: int = 5) -> dict:
+    """An output cotangent dY ~ N(0,1) of the shape of the mixer's output,
+    exact in the workload's dtype: {"dY": float32 values, "dY_bits": uint16
+    (bf16 only)}."""
+    s = wl.shape
+    hb, hv = _round(normal(seed, STREAM_DY, s.B * s.H * s.N * s.D).reshape(s.B, s.H, s.N, s.D), wl.dtype)
+    out = {"dY": hv}
+    if hb is not None:
+        out["dY_bits"] = hb
+    return out

@@ -27,7 +27,8 @@ def test_header_declares_the_boundary():
     names = _header_functions()
     for want in ("flarepp_forward", "flarepp_forward_ws", "flarepp_forward_debug",
                  "flarepp_workspace_size", "flarepp_sync_status", "flarepp_status_string",
-                 "flarepp_forward_variant", "flare_forward"):
+                 "flarepp_forward_variant", "flare_forward", "flarepp_project",
+                 "flarepp_backward"):
         assert want in names
 
 
@@ -152,3 +153,23 @@ def test_project_argument_validation_without_gpu(lib):
     assert call([2, 0, 0], o=same) == 1                 # outputs overlap
     onx = (ctypes.c_void_p * 3)(X, 0x2000000, 0x3000000)
     assert call([2, 0, 0], o=onx) == 1                  # output aliases X
+
+
+def test_backward_argument_validation_without_gpu(lib):
+    l = lib[0]
+    f = l.flarepp_backward
+    vp = ctypes.c_void_p
+    f.argtypes = [vp] * 7 + [ctypes.c_int] * 6 + [vp] * 7
+    f.restype = ctypes.c_int
+    ins = [0x100000 * (i + 1) for i in range(7)]
+    outs = [0x10000000 * (i + 1) for i in range(6)]
+
+    def call(i=ins, o=outs, M=32, D=16):
+        return f(*i, 1, 2, 64, M, D, 0, *o, None)
+
+    assert call(i=[None] + ins[1:]) == 1                 # null K
+    assert call(o=outs[:5] + [None]) == 1                # null dgate
+    assert call(D=64) == 2                               # D unsupported
+    assert call(i=ins[:6] + [ins[6] + 4]) == 3           # misaligned dY
+    assert call(o=[ins[6]] + outs[1:]) == 1              # dK aliases dY
+    assert call(o=[outs[0], outs[0]] + outs[2:]) == 1    # dK and dV overlap
