@@ -451,6 +451,86 @@ def run_project(args, rank, world, local_rank):
     }
 
 
+FP32_FMA_PER_CLK_PER_SM = 128  # CUDA-core fp32 FMA lanes per SM per clock
+
+
+def run_backward(args, rank, world, local_rank):
+    """The mixer's backward pass (all input gradients for a random output
+    cotangent) on the workload. It runs on the CUDA cores in fp32, so it is
+    reported against the fp32 FMA peak (128 FMA lanes per SM per clock x SMs x
+    the max SM clock) with 24 B H N M D algorithmic flops: each of the three
+    attention calls costs four N x M x D products backward (scores, dP, and
+    the two gradient products), twice the forward's two."""
+    import torch
+    from rank_latent_routing_gb300 import flarepp
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = workloads.config(args.workload)
+    s = wl.shape
+    dev, host = upload(wl, torch, device)
+    ct = workloads.cotangent(wl)
+    if wl.dtype == "bf16":
+        dy = torch.from_numpy(np.ascontiguousarray(ct["dY_bits"]).view(np.int16)).view(torch.bfloat16).to(device)
+    else:
+        dy = torch.from_numpy(ct["dY"]).to(device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        return flarepp.backward(dev["K"], dev["V"], dev["Ks_raw"], dev["Qseed"], dev["Qf"], dev["gate"], dy)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if flarepp.sync_status() != 0:
+        raise RuntimeError("device error during warm-up")
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    clk = clocks.stop(t0, t1)
+    if flarepp.sync_status() != 0:
+        raise RuntimeError("device error in timed region")
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    t_max = max_over_ranks([ms], world, device)[0]
+    if rank != 0:
+        return None
+    peaks, kind = load_peaks()
+    tokens = s.tokens * world
+    t = t_max * 1e-3
+    flops = 24.0 * s.B * s.H * s.N * s.M * s.D
+    peak_tf = FP32_FMA_PER_CLK_PER_SM * 2 * SMS * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    ach = flops / t / 1e12
+    return {
+        "metric": "FLARE++ mixer backward tokens/s", "value": round(tokens / t, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, shapes of the paper's workloads)",
+        "config": {"workload": f"backward of {wl.name}: B={s.B} H={s.H} N={s.N} M={s.M} D={s.D} "
+                               f"{wl.dtype} inputs, fp32 gradients",
+                   "l2": "512 MB flush before every timed step"},
+        "roofline": {"bound": "alu", "kernel": "backward passes (CUDA cores)", "achieved": round(ach, 3),
+                     "peak": round(peak_tf, 3), "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4),
+                     "traffic": None,
+                     "peak_source": "fp32 FMA: 128 lanes/clk/SM x 2 flops x 152 SMs x max SM clock"},
+        "clocks": clk,
+        "gpu_launches": 12 * args.steps,
+        "impl": "ours",
+    }
+
+
 # ------------------------------------------------------------ CPU oracle
 def _pool_init():
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -579,8 +659,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="pde2d", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="mixer", choices=["mixer", "project"],
-                    help="what to time: the mixer forward, or the fused token projections")
+    ap.add_argument("--op", default="mixer", choices=["mixer", "project", "backward"],
+                    help="what to time: the mixer forward, the fused token projections, or the "
+                         "mixer's backward pass")
     ap.add_argument("--variant", default="flarepp", choices=sorted(VARIANT_INPUTS),
                     help="mixer: FLARE++ (default), separate synthesis values, simplified "
                          "FLARE++, or FLARE")
@@ -605,7 +686,8 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        line = (run_project if args.op == "project" else run_ours)(args, rank, world, local_rank)
+        run = {"mixer": run_ours, "project": run_project, "backward": run_backward}[args.op]
+        line = run(args, rank, world, local_rank)
     finally:
         if world > 1:
             dist.destroy_process_group()
