@@ -16,9 +16,10 @@
 //    Q = N0(Qf) + g * Qd in fp32, cast to bf16. The encode instance ends with
 //    Z (bf16) and L.
 //  * decode_kernel — tokens attend over the M routes: Q and Z of the head stay
-//    in shared memory for all of the CTA's token tiles; S = K Q^T is computed
-//    128 routes at a time with an online softmax over M per token, and
-//    O += P [Z | 1]; out = O / rowsum in bf16.
+//    in shared memory for all of the CTA's token tiles; each column half of a
+//    TMEM slot owns a token tile and computes S = K Q^T 64 routes at a time
+//    with an online softmax over M per token, and O += P [Z | 1];
+//    out = O / rowsum in bf16.
 //
 // One CTA per SM, 512 threads: warp 0 issues TMA loads, warps 1-4 issue the
 // MMAs (one thread each, one per (slot, column half); warp 1 owns TMEM),
@@ -105,7 +106,10 @@ struct Shared {
   int last;
 };
 
+// A phase that has completed is taken at once; the abort flag is read only on
+// the slow path, so a wait that needs no waiting costs no shared-memory load.
 __device__ __forceinline__ bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   if (*(volatile int*)&sh.abort) return false;
   if (mbar_wait(bar, parity, kWaitLimit)) return true;
   atomicOr(&g_tc_error, kErrTimeout);
@@ -816,26 +820,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ----------------------------------------------------------- decode kernel
 struct DecodeParams {
-  int N, M, H, tiles_per_cta, stages;
+  int N, M, H, tiles_per_cta;
   int q_by_head;       // routing queries [H][M][D] (1) or [BH][M][D] (0)
   __nv_bfloat16* out;  // [BH][N][D]
 };
 
-// Exchange buffer of the decode kernel: the second column half's (L, Z) of
-// each row of both slots, read by the first half to form the output.
+// Token-tile ring depth of the decode kernel: a compile-time constant, so
+// that the ring index and phase of a tile cost no division on the issuing
+// threads. With Q and Z of M <= 512 routes resident it still fits.
+constexpr int kDecodeStages = kMaxStages;
 template <int D>
-__host__ __device__ constexpr int decode_xchg_bytes() {
-  return 2 * 128 * (D + 1) * 4;
+__host__ __device__ constexpr int decode_smem_bytes(int M) {
+  return 1024 + (2 * ((M + kTile - 1) / kTile) + kDecodeStages + 1) * (int)Layout<D>::kTileBytes;
 }
-
-// Token-tile ring depth of the decode kernel for M routes.
-template <int D>
-__host__ __device__ constexpr int decode_stages(int M) {
-  const int chunks = (M + kTile - 1) / kTile;
-  const int n = (210 * 1024 - decode_xchg_bytes<D>() - (2 * chunks + 1) * (int)Layout<D>::kTileBytes) /
-                (int)Layout<D>::kTileBytes;
-  return n > kMaxStages ? kMaxStages : n;
-}
+static_assert(decode_smem_bytes<32>(512) <= 210 * 1024, "decode ring does not fit next to Q and Z");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -847,12 +845,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   const int chunks = (p.M + kTile - 1) / kTile;
-  const int stages = p.stages;
+  constexpr int stages = kDecodeStages;
   unsigned char* sQ = smem;                                // [chunks][128][D]
   unsigned char* sZ = smem + chunks * L::kTileBytes;       // [chunks][128][D]
   unsigned char* sK = smem + 2 * chunks * L::kTileBytes;   // [stages][128][D]
   unsigned char* sOnes = sK + stages * L::kTileBytes;      // [128][D]
-  float* xchg = reinterpret_cast<float*>(sOnes + L::kTileBytes);  // [2][128][D + 1]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -860,31 +857,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (p.N + kTile - 1) / kTile;
   const int t_begin = blockIdx.x * p.tiles_per_cta;
   const int T = max(0, min(n_tiles, t_begin + p.tiles_per_cta) - t_begin);
-  // Two schedules. With M <= 64 routes (`pairs`) a step of slot k holds two
-  // token tiles, one per column half: step u of slot k takes tiles 2g and
-  // 2g + 1 with g = 2u + k, every half its own tile over all M routes, so a
-  // half's accumulator is a whole output row. Otherwise slot k takes local
-  // tiles k, k+2, ..., each in `chunks` steps of 128 routes, and the two
-  // halves (routes 0-63 and 64-127 of a block) are merged per token at the
-  // end of the tile.
-  const bool pairs = p.M <= 64;
+  // Schedule: each column half of a slot owns whole token tiles and runs over
+  // all M routes of its tile in `nsub` steps of 64 routes, carrying its online
+  // softmax over M from one step to the next, so its accumulator ends as a
+  // whole output row and the two halves never exchange data. Step u of slot k
+  // works on tile pair g = 2 (u / nsub) + k: half hf takes local tile
+  // 2g + hf, routes 64 (u % nsub) .. +63.
+  const int nsub = (p.M + 63) / 64;
   int steps[2];
-  for (int k = 0; k < 2; ++k) {
-    if (pairs) {
-      const int G = (T + 1) / 2;
-      steps[k] = G > k ? (G - k + 1) / 2 : 0;
-    } else {
-      steps[k] = T > k ? ((T - k + 1) / 2) * chunks : 0;
-    }
+  {
+    const int G = (T + 1) / 2;
+    for (int k = 0; k < 2; ++k) steps[k] = (G > k ? (G - k + 1) / 2 : 0) * nsub;
   }
   const int umax = max(steps[0], steps[1]);
-  // local token tile of half hf of slot k's step u (may be past T in pairs mode)
-  auto tile_of = [&](int k, int u, int hf) { return pairs ? 2 * (2 * u + k) + hf : k + 2 * (u / chunks); };
+  // local token tile of half hf of slot k's step u (may be past T when T is odd)
+  auto tile_of = [&](int k, int u, int hf) { return 2 * (2 * (u / nsub) + k) + hf; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], pairs ? 1 : 2);  // one release per issuing thread that reads the tile
+      mbar_init(&sh.empty[s], 1);  // a tile is read by one issuing thread
     }
     mbar_init(&sh.q_full, 1);
     for (int k = 0; k < 2; ++k)
@@ -935,49 +927,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kWarpNorm) {
     if (lane == 0) {
       const int kk = (warp - kWarpIssue) >> 1, hf = (warp - kWarpIssue) & 1;
-      const uint32_t aQ = smem_u32(sQ), aZ = smem_u32(sZ), aOnes = smem_u32(sOnes);
+      const uint32_t aZ = smem_u32(sZ), aOnes = smem_u32(sOnes);
       const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
-      // scores of the half for slot kk's step u: pairs mode, all M routes of
-      // the half's own tile; otherwise routes 64hf .. 64hf+63 of block u % chunks
       // descriptors built once; an MMA moves them with one add (a thread
-      // spends its issue slots on every instruction between MMAs)
+      // spends its issue slots on every instruction between MMAs). Routes
+      // 64b .. 64b+63 start 64b rows into the chunked Q (and Z) tiles.
       const uint64_t dK0 = L::kmajor(smem_u32(sK), 0);
-      const uint64_t dQ0 = L::kmajor(aQ + (pairs ? 0u : hf * 64u * L::kRowBytes), 0);
+      const uint64_t dQ0 = L::kmajor(smem_u32(sQ), 0);
       const uint32_t idS64 = idesc_bf16(128, 64, false, false);
       const uint32_t dS = tmem + kk * kSlotCols + 64 * hf;
       const uint32_t dO = tmem + kk * kSlotCols + kColO + hf * L::kNo;
-      // scores of the half for slot kk's step u: pairs mode, all M routes of
-      // the half's own tile; otherwise routes 64hf .. 64hf+63 of block u % chunks
-      auto issue_s = [&](int u) -> bool {
-        const int t = tile_of(kk, u, hf), ch = pairs ? 0 : u % chunks;
+      // scores of local tile t against routes 64b .. 64b+63
+      auto issue_s = [&](int t, int b) -> bool {
         if (t < T) {
           const int s = t % stages;
-          if (ch == 0) {
+          if (b == 0) {
             if (!wait_or_abort(sh, &sh.full[s], (t / stages) & 1)) return false;
             tc_fence_after();
           }
-          const int width = pairs ? p.M : min(kTile, p.M - ch * kTile) - 64 * hf;
-          if (width > 0) {
-            const uint64_t a = L::adv(dK0, s * L::kTileBytes), b = L::adv(dQ0, ch * L::kTileBytes);
-            const uint32_t id = width >= 64 ? idS64 : idesc_bf16(128, width, false, false);
+          const int width = min(64, p.M - 64 * b);
+          const uint64_t a = L::adv(dK0, s * L::kTileBytes), bq = L::adv(dQ0, b * 64 * L::kRowBytes);
+          const uint32_t id = width >= 64 ? idS64 : idesc_bf16(128, width, false, false);
 #pragma unroll
-            for (int q = 0; q < D / 16; ++q) mma_ss(dS, L::adv(a, 32 * q), L::adv(b, 32 * q), id, q > 0);
-          }
-          if (ch == chunks - 1) mma_commit(&sh.empty[s]);
+          for (int q = 0; q < D / 16; ++q) mma_ss(dS, L::adv(a, 32 * q), L::adv(bq, 32 * q), id, q > 0);
+          if (b == nsub - 1) mma_commit(&sh.empty[s]);
         }
         mma_commit(&sh.s_full[kk][hf]);
         return true;
       };
-      // O_hf += P_hf [Z | 1] over the half's route slices
-      auto issue_pv = [&](int u) {
-        if (tile_of(kk, u, hf) >= T) return;
-        const int ch = pairs ? 0 : u % chunks;
-        const int nsl = pairs ? p.M / 16 : min(4, min(kTile, p.M - ch * kTile) / 16 - 4 * hf);
-        const int sl0 = pairs ? 0 : 4 * hf;  // first route slice of the half
-        const uint32_t zc = aZ + ch * L::kTileBytes;
-        const uint64_t v = L::values1(zc, aOnes, sl0);
+      // O_hf (+)= P_hf [Z | 1] over the route slices of block b
+      auto issue_pv = [&](int t, int b) {
+        if (t >= T) return;
+        const int nsl = min(64, p.M - 64 * b) / 16;
+        const uint64_t v = L::values1(aZ + (b >> 1) * L::kTileBytes, aOnes, 4 * (b & 1));
         const uint32_t aP = tmem + kk * kSlotCols + 64 * hf;
-        const uint32_t first = ch > 0 ? 1u : 0u;
+        const uint32_t first = b > 0 ? 1u : 0u;
         if (nsl == 4) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) mma_ts(dO, aP + i * 8, L::adv(v, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
@@ -985,13 +969,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < nsl; ++i) mma_ts(dO, aP + i * 8, L::adv(v, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
         }
       };
+      // the step's tile and route block, advanced without a division
+      int t = tile_of(kk, 0, hf), b = 0;
       bool ok = steps[kk] > 0 && wait_or_abort(sh, &sh.q_full, 0);
-      if (ok) ok = issue_s(0);
+      if (ok) ok = issue_s(t, b);
       for (int u = 0; ok && u < steps[kk]; ++u) {
         if (!wait_or_abort(sh, &sh.p_full[kk][hf], u & 1)) break;
         tc_fence_after();
-        issue_pv(u);
-        if (u + 1 < steps[kk]) ok = issue_s(u + 1);
+        issue_pv(t, b);
+        if (++b == nsub) {
+          b = 0;
+          t += 4;
+        }
+        if (u + 1 < steps[kk]) ok = issue_s(t, b);
         else mma_commit(&sh.o_full[kk][hf]);
       }
       mma_commit(&sh.drain);
@@ -1005,10 +995,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = rsqrtf((float)D) * kLog2e;
     float r[2] = {-INFINITY, -INFINITY}, ro[2] = {-INFINITY, -INFINITY};
     bool acc[2] = {false, false};
-    // out = O / rowsum of this half's accumulator, for its own token tile
-    // (pairs mode: no exchange)
-    auto emit_own = [&](int k, int u, bool live) {
-      const int t = tile_of(k, u, hf);
+    // out = O / rowsum of this half's accumulator, for its own token tile t
+    auto emit = [&](int k, int t, bool live) {
       if (!live || t >= T) return;
       float z[D];
       const float l = load_acc<D>(tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo, z);
@@ -1020,63 +1008,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         store_row<D>(p.out + ((size_t)bh * p.N + tok) * D, z);
       }
     };
-    // out = the two halves' (L, Z) merged, for the token tile of slot k's step
-    // u. Every softmax thread calls it at the same points of the schedule,
-    // also after a failed wait (`live` false), so that the exchange barrier
-    // inside always completes.
-    auto emit_merged = [&](int k, int u, bool live) {
-      const int t = tile_of(k, u, 0);
-      float z[D];
-      const float l = load_acc<D>(tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo, z);
-      const bool any = live && acc[k] && l > 0.f;
-      const float lg = any ? ro[k] + __log2f(l) : -INFINITY;  // exp2 units
-      const float inv = any ? 1.f / l : 0.f;
-      float* xr = xchg + (k * 128 + row) * (D + 1);
-      if (hf == 1) {
-        xr[0] = lg;
-#pragma unroll
-        for (int d = 0; d < D; ++d) xr[1 + d] = z[d] * inv;
-      }
-      softmax_groups_sync();
-      if (hf == 0 && live) {
-        const float lb = xr[0];
-        const float m = fmaxf(lg, lb);
-        const float wa = lg == -INFINITY ? 0.f : exp2f(lg - m);
-        const float wb = lb == -INFINITY ? 0.f : exp2f(lb - m);
-        const float inv_w = 1.f / (wa + wb);
-        const int tok = (t_begin + t) * kTile + row;
-        if (tok < p.N) {
-#pragma unroll
-          for (int d = 0; d < D; ++d) z[d] = (wa * z[d] * inv + wb * xr[1 + d]) * inv_w;
-          store_row<D>(p.out + ((size_t)bh * p.N + tok) * D, z);
-        }
-      }
-    };
     bool ok = true;
+    // the step's route block (the same for both slots) and each slot's tile
+    int b = 0;
+    int tk[2] = {tile_of(0, 0, hf), tile_of(1, 0, hf)};
     for (int u = 0; u < umax; ++u) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         if (u >= steps[k]) continue;
         const uint32_t tS = tmem + lane_base + k * kSlotCols + 64 * hf;
         const uint32_t tO = tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo;
-        const int ch = pairs ? 0 : u % chunks;
         ok = ok && wait_or_abort(sh, &sh.s_full[k][hf], u & 1);
         tc_fence_after();
-        if (ch == 0) {
+        if (b == 0) {
           // the previous tile's products are in: its output goes out before
-          // this step's products overwrite the accumulators
-          if (u > 0) {
-            if (pairs) emit_own(k, u - 1, ok);
-            else emit_merged(k, u - 1, ok);
-          }
+          // this step's products overwrite the accumulator
+          if (u > 0) emit(k, tk[k] - 4, ok);
           r[k] = -INFINITY;
           acc[k] = false;
         }
         if (!ok) continue;
-        const int valid = pairs ? (tile_of(k, u, hf) < T ? p.M : 0) : min(kTile, p.M - ch * kTile) - 64 * hf;
-        if (valid > 0) softmax_half(tS, min(valid, 64), c, r[k]);
+        const int valid = tk[k] < T ? min(64, p.M - 64 * b) : 0;
+        if (valid > 0) softmax_half(tS, valid, c, r[k]);
         finish_half<D>(&sh.p_full[k][hf], tO, r[k], ro[k], acc[k]);
         if (valid > 0) acc[k] = true;
+      }
+      if (++b == nsub) {
+        b = 0;
+        tk[0] += 4;
+        tk[1] += 4;
       }
     }
     // the last tile of each slot
@@ -1085,8 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (steps[k] == 0) continue;
       const bool done = ok && wait_or_abort(sh, &sh.o_full[k][hf], 0);
       tc_fence_after();
-      if (pairs) emit_own(k, steps[k] - 1, done);
-      else emit_merged(k, steps[k] - 1, done);
+      emit(k, tile_of(k, steps[k] - 1, hf), done);
     }
   }
   tc_fence_before();
@@ -1104,8 +1063,7 @@ size_t split_smem() {
 
 template <int D>
 size_t decode_smem(int M) {
-  const int chunks = (M + kTile - 1) / kTile;
-  return 1024 + (2 * chunks + decode_stages<D>(M) + 1) * (size_t)Layout<D>::kTileBytes + decode_xchg_bytes<D>();
+  return (size_t)decode_smem_bytes<D>(M);
 }
 
 template <int D, int kKind>
@@ -1192,7 +1150,6 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
   {
     DecodeParams d{};
     d.N = pr.N; d.M = pr.M; d.H = pr.H; d.tiles_per_cta = pl.decode_tiles_per_cta;
-    d.stages = decode_stages<D>(pr.M);
     d.q_by_head = flare ? 1 : 0;
     d.out = static_cast<__nv_bfloat16*>(pr.out);
     const size_t smem = decode_smem<D>(pr.M);

@@ -50,6 +50,8 @@ CASES = [
     ("iid", 1, 2, 129, 48, 16, "bf16"),
     ("iid", 1, 1, 1, 64, 32, "bf16"),        # N = 1
     ("iid", 1, 2, 5000, 192, 16, "bf16"),    # M not a multiple of 128
+    ("iid", 1, 2, 2000, 80, 32, "bf16"),     # last 64-route block of the decode has 16 routes
+    ("lowrank", 2, 1, 1500, 144, 16, "bf16"),  # two latent blocks, the second 16 rows; ragged route block
 ]
 
 
