@@ -43,7 +43,9 @@ struct DeviceProblem {
 // row): 1, the token streams inside a CTA being merged before the write.
 struct TcPlan {
   int tiles, qgroups, splits, split_len, streams;
-  int decode_ctas_per_head, decode_tiles_per_cta;
+  // decode: tiles per CTA; CTAs per head (0: CTAs walk the flattened
+  // (head, tile) order); Q/Z slots per CTA; grid size
+  int decode_tiles_per_cta, decode_ctas_per_head, decode_heads, decode_ctas;
 };
 
 // Workspace regions (device pointers into the caller's or the cache's buffer).

@@ -59,6 +59,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -820,7 +821,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ----------------------------------------------------------- decode kernel
 struct DecodeParams {
-  int N, M, H, tiles_per_cta;
+  int N, M, H, BH;
+  int tiles_per_cta;   // consecutive token tiles per CTA
+  int ctas_per_head;   // > 0: a CTA's tiles lie in one head; 0: tiles in flattened (head, tile) order
+  int heads;           // Q/Z slots in shared memory: the most heads one CTA's tiles span
   int q_by_head;       // routing queries [H][M][D] (1) or [BH][M][D] (0)
   __nv_bfloat16* out;  // [BH][N][D]
 };
@@ -829,11 +833,14 @@ struct DecodeParams {
 // that the ring index and phase of a tile cost no division on the issuing
 // threads. With Q and Z of M <= 512 routes resident it still fits.
 constexpr int kDecodeStages = kMaxStages;
+// At most this many heads' Q and Z per CTA, within this much shared memory.
+constexpr int kDecodeHeads = 4;
+constexpr int kDecodeSmemLimit = 220 * 1024;
 template <int D>
-__host__ __device__ constexpr int decode_smem_bytes(int M) {
-  return 1024 + (2 * ((M + kTile - 1) / kTile) + kDecodeStages + 1) * (int)Layout<D>::kTileBytes;
+__host__ __device__ constexpr int decode_smem_bytes(int M, int heads) {
+  return 1024 + (2 * heads * ((M + kTile - 1) / kTile) + kDecodeStages + 1) * (int)Layout<D>::kTileBytes;
 }
-static_assert(decode_smem_bytes<32>(512) <= 210 * 1024, "decode ring does not fit next to Q and Z");
+static_assert(decode_smem_bytes<32>(512, 1) <= kDecodeSmemLimit, "decode ring does not fit next to Q and Z");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -845,18 +852,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   const int chunks = (p.M + kTile - 1) / kTile;
+  const uint32_t head_bytes = chunks * L::kTileBytes;      // Q (or Z) of one head
   constexpr int stages = kDecodeStages;
-  unsigned char* sQ = smem;                                // [chunks][128][D]
-  unsigned char* sZ = smem + chunks * L::kTileBytes;       // [chunks][128][D]
-  unsigned char* sK = smem + 2 * chunks * L::kTileBytes;   // [stages][128][D]
+  unsigned char* sQ = smem;                                // [heads][chunks][128][D]
+  unsigned char* sZ = smem + p.heads * head_bytes;         // [heads][chunks][128][D]
+  unsigned char* sK = smem + 2 * p.heads * head_bytes;     // [stages][128][D]
   unsigned char* sOnes = sK + stages * L::kTileBytes;      // [128][D]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
+  // The CTA's token tiles: T consecutive tiles of the flattened (head, tile)
+  // order, from tile `first` of head h0. They span `nheads` heads, whose Q and
+  // Z all stay resident; local tile t belongs to head h0 + head_slot(t).
   const int n_tiles = (p.N + kTile - 1) / kTile;
-  const int t_begin = blockIdx.x * p.tiles_per_cta;
-  const int T = max(0, min(n_tiles, t_begin + p.tiles_per_cta) - t_begin);
+  long long g0;
+  int T;
+  if (p.ctas_per_head > 0) {
+    const int hh = blockIdx.x / p.ctas_per_head, j = blockIdx.x - hh * p.ctas_per_head;
+    g0 = (long long)hh * n_tiles + (long long)j * p.tiles_per_cta;
+    T = max(0, min(p.tiles_per_cta, n_tiles - j * p.tiles_per_cta));
+  } else {
+    g0 = (long long)blockIdx.x * p.tiles_per_cta;
+    T = (int)max(0LL, min((long long)p.tiles_per_cta, (long long)p.BH * n_tiles - g0));
+  }
+  const int h0 = (int)(g0 / n_tiles);
+  const int first = (int)(g0 - (long long)h0 * n_tiles);
+  const int nheads = T > 0 ? (first + T - 1) / n_tiles + 1 : 1;
+  if (nheads > p.heads) {
+    // more heads than the plan made room for: record it, run nothing
+    if (threadIdx.x == 0) atomicOr(&g_tc_error, kErrBadState);
+    return;
+  }
+  int bnd[kDecodeHeads];  // first local tile of head slot i >= 1; past every tile when absent
+#pragma unroll
+  for (int i = 0; i < kDecodeHeads; ++i) bnd[i] = i > 0 && i < nheads ? i * n_tiles - first : INT_MAX;
+  auto head_slot = [&](int t) {
+    int hs = 0;
+#pragma unroll
+    for (int i = 1; i < kDecodeHeads; ++i) hs += t >= bnd[i] ? 1 : 0;
+    return hs;
+  };
   // Schedule: each column half of a slot owns whole token tiles and runs over
   // all M routes of its tile in `nsub` steps of 64 routes, carrying its online
   // softmax over M from one step to the next, so its accumulator ends as a
@@ -905,17 +940,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_z);
-      mbar_arrive_expect_tx(&sh.q_full, 2 * chunks * L::kTileBytes);
-      for (int ch = 0; ch < chunks; ++ch) {
-        tma_load_3d(sQ + ch * L::kTileBytes, &tm_q, &sh.q_full, 0, ch * kTile, p.q_by_head ? bh % p.H : bh);
-        tma_load_3d(sZ + ch * L::kTileBytes, &tm_z, &sh.q_full, 0, ch * kTile, bh);
+      mbar_arrive_expect_tx(&sh.q_full, 2 * nheads * head_bytes);
+      for (int hs = 0; hs < nheads; ++hs) {
+        const int bh = h0 + hs;
+        for (int ch = 0; ch < chunks; ++ch) {
+          const uint32_t off = hs * head_bytes + ch * L::kTileBytes;
+          tma_load_3d(sQ + off, &tm_q, &sh.q_full, 0, ch * kTile, p.q_by_head ? bh % p.H : bh);
+          tma_load_3d(sZ + off, &tm_z, &sh.q_full, 0, ch * kTile, bh);
+        }
       }
       int issued = 0;
       for (int t = 0; t < T; ++t) {
         const int s = t % stages;
         if (t >= stages && !wait_or_abort(sh, &sh.empty[s], ((t / stages) - 1) & 1)) break;
+        const int hs = head_slot(t);
         mbar_arrive_expect_tx(&sh.full[s], L::kTileBytes);
-        tma_load_3d(sK + s * L::kTileBytes, &tm_k, &sh.full[s], 0, (t_begin + t) * kTile, bh);
+        tma_load_3d(sK + s * L::kTileBytes, &tm_k, &sh.full[s], 0, (first + t - hs * n_tiles) * kTile, h0 + hs);
         issued = t + 1;
       }
       if (*(volatile int*)&sh.abort) {
@@ -937,8 +977,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idS64 = idesc_bf16(128, 64, false, false);
       const uint32_t dS = tmem + kk * kSlotCols + 64 * hf;
       const uint32_t dO = tmem + kk * kSlotCols + kColO + hf * L::kNo;
-      // scores of local tile t against routes 64b .. 64b+63
-      auto issue_s = [&](int t, int b) -> bool {
+      // scores of local tile t against routes 64b .. 64b+63 of its head, whose
+      // Q and Z sit `hoff` bytes into their arrays
+      auto issue_s = [&](int t, int b, uint32_t hoff) -> bool {
         if (t < T) {
           const int s = t % stages;
           if (b == 0) {
@@ -946,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
           }
           const int width = min(64, p.M - 64 * b);
-          const uint64_t a = L::adv(dK0, s * L::kTileBytes), bq = L::adv(dQ0, b * 64 * L::kRowBytes);
+          const uint64_t a = L::adv(dK0, s * L::kTileBytes), bq = L::adv(dQ0, hoff + b * 64 * L::kRowBytes);
           const uint32_t id = width >= 64 ? idS64 : idesc_bf16(128, width, false, false);
 #pragma unroll
           for (int q = 0; q < D / 16; ++q) mma_ss(dS, L::adv(a, 32 * q), L::adv(bq, 32 * q), id, q > 0);
@@ -956,10 +997,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       // O_hf (+)= P_hf [Z | 1] over the route slices of block b
-      auto issue_pv = [&](int t, int b) {
+      auto issue_pv = [&](int t, int b, uint32_t hoff) {
         if (t >= T) return;
         const int nsl = min(64, p.M - 64 * b) / 16;
-        const uint64_t v = L::values1(aZ + (b >> 1) * L::kTileBytes, aOnes, 4 * (b & 1));
+        const uint64_t v = L::values1(aZ + hoff + (b >> 1) * L::kTileBytes, aOnes, 4 * (b & 1));
         const uint32_t aP = tmem + kk * kSlotCols + 64 * hf;
         const uint32_t first = b > 0 ? 1u : 0u;
         if (nsl == 4) {
@@ -971,17 +1012,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // the step's tile and route block, advanced without a division
       int t = tile_of(kk, 0, hf), b = 0;
+      uint32_t hoff = head_slot(t) * head_bytes;
       bool ok = steps[kk] > 0 && wait_or_abort(sh, &sh.q_full, 0);
-      if (ok) ok = issue_s(t, b);
+      if (ok) ok = issue_s(t, b, hoff);
       for (int u = 0; ok && u < steps[kk]; ++u) {
         if (!wait_or_abort(sh, &sh.p_full[kk][hf], u & 1)) break;
         tc_fence_after();
-        issue_pv(t, b);
+        issue_pv(t, b, hoff);
         if (++b == nsub) {
           b = 0;
           t += 4;
+          hoff = head_slot(t) * head_bytes;
         }
-        if (u + 1 < steps[kk]) ok = issue_s(t, b);
+        if (u + 1 < steps[kk]) ok = issue_s(t, b, hoff);
         else mma_commit(&sh.o_full[kk][hf]);
       }
       mma_commit(&sh.drain);
@@ -1000,12 +1043,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!live || t >= T) return;
       float z[D];
       const float l = load_acc<D>(tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo, z);
-      const int tok = (t_begin + t) * kTile + row;
+      const int hs = head_slot(t);
+      const int tok = (first + t - hs * n_tiles) * kTile + row;
       if (tok < p.N) {
         const float inv = 1.f / l;
 #pragma unroll
         for (int d = 0; d < D; ++d) z[d] *= inv;
-        store_row<D>(p.out + ((size_t)bh * p.N + tok) * D, z);
+        store_row<D>(p.out + ((size_t)(h0 + hs) * p.N + tok) * D, z);
       }
     };
     bool ok = true;
@@ -1062,8 +1106,8 @@ size_t split_smem() {
 }
 
 template <int D>
-size_t decode_smem(int M) {
-  return (size_t)decode_smem_bytes<D>(M);
+size_t decode_smem(int M, int heads) {
+  return (size_t)decode_smem_bytes<D>(M, heads);
 }
 
 template <int D, int kKind>
@@ -1149,15 +1193,18 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
   // decode (a6)
   {
     DecodeParams d{};
-    d.N = pr.N; d.M = pr.M; d.H = pr.H; d.tiles_per_cta = pl.decode_tiles_per_cta;
+    d.N = pr.N; d.M = pr.M; d.H = pr.H; d.BH = BH;
+    d.tiles_per_cta = pl.decode_tiles_per_cta;
+    d.ctas_per_head = pl.decode_ctas_per_head;
+    d.heads = pl.decode_heads;
     d.q_by_head = flare ? 1 : 0;
     d.out = static_cast<__nv_bfloat16*>(pr.out);
-    const size_t smem = decode_smem<D>(pr.M);
+    const size_t smem = decode_smem<D>(pr.M, pl.decode_heads);
     *failed = "cudaFuncSetAttribute(decode)";
     if ((e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
         cudaSuccess)
       return e;
-    decode_kernel<D><<<dim3(pl.decode_ctas_per_head, BH), kThreads, smem, stream>>>(m_k, m_qdec, m_zdec, d);
+    decode_kernel<D><<<pl.decode_ctas, kThreads, smem, stream>>>(m_k, m_qdec, m_zdec, d);
     *failed = "launch decode";
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -1191,7 +1238,6 @@ int choose_splits(long long groups, int n_tiles, int sms, int min_tiles, int ove
 }  // namespace tc
 
 TcPlan tc_plan(int B, int H, int N, int M, int D, int sms, int forced_splits) {
-  (void)D;
   TcPlan pl{};
   const long long BH = (long long)B * H;
   const int n_tiles = (N + tc::kTile - 1) / tc::kTile;
@@ -1203,11 +1249,27 @@ TcPlan tc_plan(int B, int H, int N, int M, int D, int sms, int forced_splits) {
   const int tiles_per_split = (n_tiles + splits - 1) / splits;
   pl.split_len = tiles_per_split * tc::kTile;
   pl.splits = (N + pl.split_len - 1) / pl.split_len;
-  // decode: one CTA per SM over consecutive token tiles of one head
-  const int dsplit = tc::choose_splits(BH, n_tiles, std::max(1, sms), 2, 4, 0);
-  const int per = (n_tiles + dsplit - 1) / dsplit;
-  pl.decode_tiles_per_cta = per;
-  pl.decode_ctas_per_head = (n_tiles + per - 1) / per;
+  // decode: one CTA per SM over consecutive token tiles. In the flattened
+  // (head, tile) order every SM gets the same number of tiles, if each CTA
+  // has room for the Q and Z of every head its tiles span; otherwise a CTA's
+  // tiles stay within one head, split by the same cost model as the encode.
+  const long long total = BH * n_tiles;
+  const int per_flat = (int)std::max(2LL, (total + std::max(1, sms) - 1) / std::max(1, sms));
+  const int heads_flat = (per_flat - 1 + n_tiles - 1) / n_tiles + 1;
+  const int smem_flat = D == 16 ? tc::decode_smem_bytes<16>(M, heads_flat) : tc::decode_smem_bytes<32>(M, heads_flat);
+  if (heads_flat <= tc::kDecodeHeads && smem_flat <= tc::kDecodeSmemLimit) {
+    pl.decode_tiles_per_cta = per_flat;
+    pl.decode_ctas_per_head = 0;
+    pl.decode_heads = heads_flat;
+    pl.decode_ctas = (int)((total + per_flat - 1) / per_flat);
+  } else {
+    const int dsplit = tc::choose_splits(BH, n_tiles, std::max(1, sms), 2, 4, 0);
+    const int per = (n_tiles + dsplit - 1) / dsplit;
+    pl.decode_tiles_per_cta = per;
+    pl.decode_ctas_per_head = (n_tiles + per - 1) / per;
+    pl.decode_heads = 1;
+    pl.decode_ctas = (int)(BH * pl.decode_ctas_per_head);
+  }
   return pl;
 }
 

@@ -52,6 +52,7 @@ CASES = [
     ("iid", 1, 2, 5000, 192, 16, "bf16"),    # M not a multiple of 128
     ("iid", 1, 2, 2000, 80, 32, "bf16"),     # last 64-route block of the decode has 16 routes
     ("lowrank", 2, 1, 1500, 144, 16, "bf16"),  # two latent blocks, the second 16 rows; ragged route block
+    ("iid", 80, 4, 100, 32, 16, "bf16"),     # 320 heads of one tile: each decode CTA spans three heads
 ]
 
 
