@@ -515,21 +515,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
       const uint32_t rows_off = hf * 64 * L::kRowBytes;  // first token row of the half in a tile
       constexpr uint32_t kLo = 0u, kAll = 0xFFFFFFFFu;
-      auto stage_addr = [&](int t) { return smem_u32(sStage + (t % kStages) * kStageBytes); };
+      // The plan in scalars (a slot index only known at run time would put the
+      // plan in local memory, and every step would wait for an L1 load):
+      // slot kk's step j works on tile t0 + dt * j (in the lanes mode lanes
+      // 64-127 take the next tile as well).
+      const bool lanes = sp.mode == kLanes;
+      const int nsteps = kk ? sp.steps[1] : sp.steps[0];
+      const int t0 = lanes ? 2 * kk : (sp.mode == kStreams ? kk : 0);
+      const int dt = lanes ? 4 : (sp.mode == kStreams ? 2 : 1);
+      const uint32_t dS = tmem + kk * kSlotCols + 64 * hf;
+      const uint32_t tQ = tmem + kk * kSlotCols + kColQ;
+      const uint32_t dO = tmem + kk * kSlotCols + kColO + hf * L::kNo;
+      const uint32_t aP = tmem + kk * kSlotCols + 64 * hf;
       auto ready = [&](int t) -> bool {
         return wait_or_abort(sh, kNormKeys ? &sh.norm[t % kStages] : &sh.full[t % kStages], (t / kStages) & 1);
       };
-      // key descriptor of the half's rows in stage 0; a stage is kStageBytes further
+      // Descriptors of stage 0, built once; stage s is s * kStageBytes further:
+      // the key descriptor's start address moves by that much, and so does the
+      // value descriptor's, whose distance to the ones tile (its leading byte
+      // offset field) shrinks by as much. Both fields stay in range, so one
+      // 64-bit add per stage moves them.
       const uint64_t dK0 = L::kmajor(smem_u32(sStage) + rows_off, 0);
-      auto key_desc = [&](int t) { return L::adv(dK0, (t % kStages) * kStageBytes); };
-      // scores of the half's 64 token columns of slot k, step j; the latent
-      // queries (A) are read from TMEM, the keys (B) from the staged tile
-      auto issue_s = [&](int k, int j) -> bool {
-        const uint32_t dS = tmem + k * kSlotCols + 64 * hf;
-        const uint32_t tQ = tmem + k * kSlotCols + kColQ;
-        const int t = slot_tile(sp, k, j);
+      const uint64_t dV0 = L::values1(smem_u32(sStage) + kValueOff, aOnes, 4 * hf);
+      constexpr uint64_t kStep = kStageBytes >> 4;
+      constexpr uint64_t kVStep = kStep - (kStep << 16);  // modulo 2^64
+      auto key_desc = [&](int t) { return dK0 + static_cast<uint64_t>(t % kStages) * kStep; };
+      auto val_desc = [&](int t) { return dV0 + static_cast<uint64_t>(t % kStages) * kVStep; };
+      // scores of the half's 64 token columns of tile t (and t + 1 in the
+      // lanes mode); the latent queries (A) are read from TMEM, the keys (B)
+      // from the staged tile
+      auto issue_s = [&](int t) -> bool {
         if (!ready(t)) return false;
-        if (sp.mode == kLanes) {
+        if (lanes) {
           const bool has_b = t + 1 < T;
           if (has_b && !ready(t + 1)) return false;
           tc_fence_after();
@@ -549,25 +566,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < D / 16; ++q) mma_ts(dS, tQ + q * 8, L::adv(ka, 32 * q), idS, q > 0);
         }
-        mma_commit(&sh.s_full[k][hf]);
+        mma_commit(&sh.s_full[kk][hf]);
         return true;
       };
-      // O_hf += P_hf [V | 1]_hf for slot k, step j: slices 4hf .. 4hf+3 of the
-      // tile, P of the half at column 64hf of the slot
-      auto issue_pv = [&](int k, int j) {
-        const uint32_t dO = tmem + k * kSlotCols + kColO + hf * L::kNo;
-        const uint32_t aP = tmem + k * kSlotCols + 64 * hf;
-        const int t = slot_tile(sp, k, j);
-        const uint32_t first = j > 0 ? 1u : 0u;
-        const uint64_t va = L::values1(stage_addr(t) + kValueOff, aOnes, 4 * hf);
-        if (sp.mode == kLanes) {
+      // O_hf (+)= P_hf [V | 1]_hf for tile t (and t + 1): slices 4hf .. 4hf+3
+      // of the tile, P of the half at column 64hf of the slot
+      auto issue_pv = [&](int t, uint32_t first) {
+        const uint64_t va = val_desc(t);
+        if (lanes) {
           const bool has_b = t + 1 < T;
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             mma_ts_masked(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kLo, kLo, kAll,
                           kAll);
           if (has_b) {
-            const uint64_t vb = L::values1(stage_addr(t + 1) + kValueOff, aOnes, 4 * hf);
+            const uint64_t vb = val_desc(t + 1);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               mma_ts_masked(dO, aP + i * 8, L::adv(vb, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kAll, kAll, kLo,
@@ -578,22 +591,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 4; ++i) mma_ts(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
         }
       };
-      // the stage(s) of the step can be refilled once this thread's products
-      // of them are done (every issuing thread that read them releases)
-      auto release = [&](int k, int j) {
-        const int t = slot_tile(sp, k, j);
+      // the stage(s) of tile t can be refilled once this thread's products of
+      // them are done (every issuing thread that read them releases)
+      auto release = [&](int t) {
         mma_commit(&sh.empty[t % kStages]);
-        if (sp.mode == kLanes && t + 1 < T) mma_commit(&sh.empty[(t + 1) % kStages]);
+        if (lanes && t + 1 < T) mma_commit(&sh.empty[(t + 1) % kStages]);
       };
-      bool ok = sp.steps[kk] > 0 && wait_or_abort(sh, &sh.q_tmem, 0);
+      bool ok = nsteps > 0 && wait_or_abort(sh, &sh.q_tmem, 0);
       tc_fence_after();
-      if (ok) ok = issue_s(kk, 0);
-      for (int j = 0; ok && j < sp.steps[kk]; ++j) {
+      if (ok) ok = issue_s(t0);
+      for (int j = 0, t = t0; ok && j < nsteps; ++j, t += dt) {
         if (!wait_or_abort(sh, &sh.p_full[kk][hf], j & 1)) break;
         tc_fence_after();
-        issue_pv(kk, j);
-        release(kk, j);
-        if (j + 1 < sp.steps[kk]) ok = issue_s(kk, j + 1);
+        issue_pv(t, j > 0 ? 1u : 0u);
+        release(t);
+        if (j + 1 < nsteps) ok = issue_s(t + dt);
       }
       // every MMA of this CTA completes before TMEM is released
       mma_commit(&sh.drain);
@@ -698,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nent = 512 / nwriters;
       for (int e = tid; e < nwriters; e += 256) {
         const int r_w = e & 127;
-        const int qt_w = sp.mode == kPair ? sp.qt[e >> 7] : sp.qt[0];
+        const int qt_w = sp.mode == kPair && (e >> 7) ? sp.qt[1] : sp.qt[0];
         const int latent_w = qt_w * kTile + r_w;
         if (latent_w >= p.M) continue;
         float lmax = -INFINITY;
@@ -738,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows = sp.mode == kLanes ? 64 : (sp.mode == kStreams ? 128 : 256);
       const int tpr = 256 / rows;
       const int rg = tid / tpr, part = tid % tpr;
-      const int qt_f = sp.mode == kPair ? sp.qt[rg >> 7] : sp.qt[0];
+      const int qt_f = sp.mode == kPair && (rg >> 7) ? sp.qt[1] : sp.qt[0];
       const int r_f = rg & 127;
       const int latent_f = qt_f * kTile + r_f;
       const size_t base = ((size_t)bh * p.qtiles + qt_f) * p.splits * kTile + r_f;
@@ -1013,9 +1025,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the step's tile and route block, advanced without a division
       int t = tile_of(kk, 0, hf), b = 0;
       uint32_t hoff = head_slot(t) * head_bytes;
-      bool ok = steps[kk] > 0 && wait_or_abort(sh, &sh.q_full, 0);
+      const int nsteps = kk ? steps[1] : steps[0];  // no run-time array index: steps stays in registers
+      bool ok = nsteps > 0 && wait_or_abort(sh, &sh.q_full, 0);
       if (ok) ok = issue_s(t, b, hoff);
-      for (int u = 0; ok && u < steps[kk]; ++u) {
+      for (int u = 0; ok && u < nsteps; ++u) {
         if (!wait_or_abort(sh, &sh.p_full[kk][hf], u & 1)) break;
         tc_fence_after();
         issue_pv(t, b, hoff);
@@ -1024,7 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           t += 4;
           hoff = head_slot(t) * head_bytes;
         }
-        if (u + 1 < steps[kk]) ok = issue_s(t, b, hoff);
+        if (u + 1 < nsteps) ok = issue_s(t, b, hoff);
         else mma_commit(&sh.o_full[kk][hf]);
       }
       mma_commit(&sh.drain);
