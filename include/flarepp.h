@@ -275,6 +275,28 @@ void flarepp_set_splits(int splits);
  */
 void flarepp_set_stage_events(cudaEvent_t* events, int count);
 
+/*
+ * Planning hook: the launch plan that flarepp_forward would use for these
+ * sizes on a GPU with `sms` multiprocessors, computed on the host without
+ * touching a device (for tests and tuning; the FLARE++ paper has no
+ * counterpart). Writes min(n, 8) values to `fields`:
+ *   [0] token splits per (batch, head, latent group) of the synthesis and
+ *       encode passes (respects flarepp_set_splits);
+ *   [1] tokens per split (a multiple of the 128-token tile on the bf16 path);
+ *   [2] latent groups per (batch, head): CTAs that split the M latent rows;
+ *   [3] consecutive 128-token tiles per decode CTA;
+ *   [4] decode CTAs per (batch, head), or 0 when the decode CTAs walk the
+ *       flattened (batch, head, tile) order and may span heads;
+ *   [5] heads whose Q and Z one decode CTA keeps in shared memory;
+ *   [6] decode CTAs in all;
+ *   [7] workspace bytes (as flarepp_workspace_size), clamped to INT_MAX.
+ * Fields [2]-[6] are 0 on the fp32 path, whose kernels plan differently.
+ * Returns FLAREPP_OK, FLAREPP_ERR_INVALID_ARG (fields NULL, n < 1 or
+ * sms < 1) or the size check's status (FLAREPP_ERR_UNSUPPORTED, ...).
+ */
+flarepp_status_t flarepp_plan_info(int B, int H, int N, int M, int D, flarepp_dtype_t dtype,
+                                   int sms, int* fields, int n);
+
 #ifdef __cplusplus
 }
 #endif

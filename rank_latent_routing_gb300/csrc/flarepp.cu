@@ -3,8 +3,9 @@
 // ABI of include/flarepp.h.
 #include <cuda_runtime.h>
 
-#include <cstdio>
 #include <algorithm>
+#include <climits>
+#include <cstdio>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -377,6 +378,25 @@ size_t flarepp_workspace_size(int B, int H, int N, int M, int D, flarepp_dtype_t
   const int sms = flarepp::device_sm_count();
   if (sms <= 0) return 0;
   return flarepp::make_plan(B, H, N, M, D, dtype, sms).total;
+}
+
+flarepp_status_t flarepp_plan_info(int B, int H, int N, int M, int D, flarepp_dtype_t dtype, int sms,
+                                   int* fields, int n) {
+  if (fields == nullptr || n < 1 || sms < 1) return FLAREPP_ERR_INVALID_ARG;
+  const flarepp_status_t st = flarepp::check_sizes(B, H, N, M, D, dtype);
+  if (st != FLAREPP_OK) return st;
+  const flarepp::Plan pl = flarepp::make_plan(B, H, N, M, D, dtype, sms);
+  const bool tc = dtype == FLAREPP_BF16;
+  const long long v[8] = {pl.splits,
+                          pl.split_len,
+                          tc ? pl.tc.qgroups : 0,
+                          tc ? pl.tc.decode_tiles_per_cta : 0,
+                          tc ? pl.tc.decode_ctas_per_head : 0,
+                          tc ? pl.tc.decode_heads : 0,
+                          tc ? pl.tc.decode_ctas : 0,
+                          (long long)std::min<size_t>(pl.total, (size_t)INT_MAX)};
+  for (int i = 0; i < n && i < 8; ++i) fields[i] = (int)v[i];
+  return FLAREPP_OK;
 }
 
 flarepp_status_t flarepp_forward_ws(const void* K, const void* V, const void* Ks_raw,

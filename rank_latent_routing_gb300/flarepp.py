@@ -74,6 +74,8 @@ def _load() -> ctypes.CDLL:
     lib.flarepp_set_splits.restype = None
     lib.flarepp_set_stage_events.argtypes = [vp, i]
     lib.flarepp_set_stage_events.restype = None
+    lib.flarepp_plan_info.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int), i]
+    lib.flarepp_plan_info.restype = ctypes.c_int
     return lib
 
 
@@ -334,6 +336,21 @@ def sync_status(stream=None) -> int:
 def set_splits(splits: int) -> None:
     """Test hook: force the token split count (0 = automatic)."""
     _lib.flarepp_set_splits(int(splits))
+
+
+PLAN_FIELDS = ("splits", "split_len", "latent_groups", "decode_tiles_per_cta",
+               "decode_ctas_per_head", "decode_heads", "decode_ctas", "workspace_bytes")
+
+
+def plan_info(B, H, N, M, D, dtype=torch.bfloat16, sms=152) -> dict:
+    """The launch plan of a forward call for these sizes on a GPU with ``sms``
+    multiprocessors, computed on the host (no device needed)."""
+    code = BF16 if dtype == torch.bfloat16 else FP32
+    arr = (ctypes.c_int * len(PLAN_FIELDS))()
+    rc = _lib.flarepp_plan_info(B, H, N, M, D, code, int(sms), arr, len(PLAN_FIELDS))
+    if rc:
+        raise FlareppError(rc, "flarepp_plan_info")
+    return dict(zip(PLAN_FIELDS, arr))
 
 
 class StageTimer:
