@@ -293,7 +293,10 @@ flarepp_status_t launch(const Problem& p, const Plan& pl, char* ws, cudaStream_t
   return launch_tc(p, pl, ws, stream);
 }
 
-// Per-(device, stream) workspace cache, stream-ordered allocation.
+// Per-(device, stream) workspace cache, stream-ordered allocation. A caller
+// holds g_cache_mu from the lookup until its kernels are enqueued: a thread
+// that grows the buffer enqueues cudaFreeAsync of the old one on the stream,
+// and a launch enqueued after that free must not use the old pointer.
 struct CachedBuf {
   void* ptr = nullptr;
   size_t bytes = 0;
@@ -301,10 +304,10 @@ struct CachedBuf {
 std::mutex g_cache_mu;
 std::map<std::pair<int, cudaStream_t>, CachedBuf> g_cache;
 
+// Caller holds g_cache_mu.
 flarepp_status_t cached_workspace(size_t bytes, cudaStream_t stream, void** out) {
   int dev = 0;
   if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice")) return FLAREPP_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_cache_mu);
   CachedBuf& buf = g_cache[{dev, stream}];
   if (buf.bytes >= bytes) {
     *out = buf.ptr;
@@ -341,8 +344,10 @@ flarepp_status_t run(const Problem& p, void* workspace, size_t ws_bytes, bool us
   }
   const Plan pl = make_plan(p.B, p.H, p.N, p.M, p.D, p.dtype, sms);
   if (use_cache) {
+    std::lock_guard<std::mutex> lock(g_cache_mu);  // until the kernels are enqueued
     st = cached_workspace(pl.total, stream, &workspace);
     if (st != FLAREPP_OK) return st;
+    return launch(p, pl, static_cast<char*>(workspace), stream);
   } else {
     if (workspace == nullptr || ws_bytes < pl.total) return FLAREPP_ERR_NO_MEMORY;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FLAREPP_ERR_ALIGNMENT;
@@ -544,6 +549,7 @@ flarepp_status_t flarepp_backward(const void* K, const void* V, const void* Ks_r
   }
   const bool bf16 = dtype == FLAREPP_BF16;
   void* ws = nullptr;
+  std::lock_guard<std::mutex> lock(flarepp::g_cache_mu);  // until the kernels are enqueued
   st = flarepp::cached_workspace(flarepp::backward_workspace_bytes(B, H, N, M, D, bf16, sms), stream, &ws);
   if (st != FLAREPP_OK) return st;
   flarepp::BwdProblem p{};
