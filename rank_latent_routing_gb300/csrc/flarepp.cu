@@ -348,10 +348,9 @@ flarepp_status_t run(const Problem& p, void* workspace, size_t ws_bytes, bool us
     st = cached_workspace(pl.total, stream, &workspace);
     if (st != FLAREPP_OK) return st;
     return launch(p, pl, static_cast<char*>(workspace), stream);
-  } else {
-    if (workspace == nullptr || ws_bytes < pl.total) return FLAREPP_ERR_NO_MEMORY;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FLAREPP_ERR_ALIGNMENT;
   }
+  if (workspace == nullptr || ws_bytes < pl.total) return FLAREPP_ERR_NO_MEMORY;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FLAREPP_ERR_ALIGNMENT;
   return launch(p, pl, static_cast<char*>(workspace), stream);
 }
 
