@@ -333,6 +333,7 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "ms_median": round(float(np.median(ms)), 5), "ms_min": round(float(min(ms)), 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic (seeded, shapes of the paper's workloads)",
         "config": {"workload": f"{wl.name}: B={s.B} H={s.H} N={s.N} M={s.M} D={s.D} {wl.dtype}"
