@@ -3,8 +3,9 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step = one full mixer forward (synthesis, gate, encode, decode) over one
-batch of the chosen synthetic workload (default: the 2-D PDE-mesh-shaped
-workload, B=4 H=8 N=16384 M=64 D=16, bf16). Prints one JSON line.
+batch of the chosen synthetic workload (default: the industrial-aero-shaped
+workload, B=1 H=8 N=1048576 M=512 D=32, bf16 -- the largest of the paper's
+workloads that fits one GPU). Prints one JSON line.
 
 Device timing: W warm-up steps, then exactly K steps, each bracketed by CUDA
 events on the launching stream, with a 512 MB L2 flush before every step
@@ -42,10 +43,17 @@ UNIT = "tokens/s"
 # Fallback denominators (used only if MEASURED_PEAKS.json is missing).
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "sm_max_mhz": 2070.0}
-SMS = 152
 # exp2 results per clock per SM on the special-function unit: 32 on GB300
-# (measured by python -m rank_latent_routing_gb300.micro; twice B200's 16)
+# (measured by python -m rank_latent_routing_gb300.micro, record in
+# profiles/issue_rates_gb300.md; twice B200's 16)
 MUFU_EX2_PER_CLK_PER_SM = 32
+
+
+def sm_count(device=None) -> int:
+    """Streaming multiprocessors of the device, read at run time."""
+    import torch
+    d = torch.cuda.current_device() if device is None else device
+    return int(torch.cuda.get_device_properties(d).multi_processor_count)
 
 
 def load_peaks():
@@ -163,19 +171,20 @@ def stage_costs(s: workloads.Shape, es: int, variant: str = "flarepp"):
     }
 
 
-def roofline(costs, stage_ms, peaks, peak_kind, clock_mhz):
+def roofline(costs, stage_ms, peaks, peak_kind, clock_mhz, sms):
     """The dominant pass against the resource that bounds it.
 
     Ideal times: bytes / HBM peak, flops / bf16 tensor peak, exps / MUFU exp2
-    peak (32 per clock per SM x 152 SMs x the max SM clock). The bound is the
-    resource with the longest ideal time; frac = that ideal time / measured.
+    peak (32 per clock per SM x the device's SMs x the max SM clock). The
+    bound is the resource with the longest ideal time; frac = that ideal time
+    / measured.
     """
     name = max(stage_ms, key=lambda k: stage_ms[k])
     c = costs[name]
     t = stage_ms[name] * 1e-3
     hbm = peaks["hbm_gbs"] * 1e9
     tensor = peaks["bf16_tflops_sustained"] * 1e12
-    exp_peak = MUFU_EX2_PER_CLK_PER_SM * SMS * peaks.get("sm_max_mhz", 2070.0) * 1e6
+    exp_peak = MUFU_EX2_PER_CLK_PER_SM * sms * peaks.get("sm_max_mhz", 2070.0) * 1e6
     ideal = {"hbm": c["bytes"] / hbm, "tensor": c["flops"] / tensor, "alu": c["exps"] / exp_peak}
     bound = max(ideal, key=lambda k: ideal[k])
     if bound == "hbm":
@@ -186,7 +195,7 @@ def roofline(costs, stage_ms, peaks, peak_kind, clock_mhz):
         ach, pk, unit = c["exps"] / t / 1e9, exp_peak / 1e9, "Gexp/s"
     return {"bound": bound, "kernel": name, "achieved": round(ach, 3), "peak": round(pk, 3),
             "unit": unit, "frac": round(ach / pk, 4), "traffic": None,
-            "peak_source": peak_kind + (" (MUFU exp2 peak: measured 32/clk/SM x 152 SMs x max "
+            "peak_source": peak_kind + (f" (MUFU exp2 peak: measured 32/clk/SM x {sms} SMs x max "
                                         "SM clock)" if bound == "alu" else ""),
             "ideal_us": {k: round(v * 1e6, 3) for k, v in ideal.items()},
             "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
@@ -205,13 +214,15 @@ def max_over_ranks(values, world, device):
     return [float(v) for v in t.tolist()]
 
 
-def measured_traffic(workload: str, kernel: str):
+TC_SOURCE = os.path.join(ROOT, "rank_latent_routing_gb300", "csrc", "tc.cu")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "roofline_traffic.md")
+
+
+def measured_traffic(workload: str, kernel: str, src: str = TC_SOURCE, prof: str = TRAFFIC_RECORD):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
     summary (profiles/roofline_traffic.md), or None when it was measured on a
     different revision of the tensor-core kernels (source hash mismatch)."""
     import hashlib
-    src = os.path.join(ROOT, "rank_latent_routing_gb300", "csrc", "tc.cu")
-    prof = os.path.join(ROOT, "profiles", "roofline_traffic.md")
     if not (os.path.exists(src) and os.path.exists(prof)):
         return None
     with open(src, "rb") as f:
@@ -225,6 +236,13 @@ def measured_traffic(workload: str, kernel: str):
                     and fields.get("source_sha1") == sha):
                 return int(fields["bytes_per_launch"])
     return None
+
+
+def workload_string(name: str, variant: str = "flarepp") -> str:
+    """The ``config.workload`` string, the same for both arms of the bench."""
+    s, dtype = workloads.CONFIGS[name][0], workloads.CONFIGS[name][1]
+    return (f"{name}: B={s.B} H={s.H} N={s.N} M={s.M} D={s.D} {dtype}"
+            + ("" if variant == "flarepp" else f", {variant} mixer"))
 
 
 def run_ours(args, rank, world, local_rank):
@@ -336,14 +354,13 @@ def run_ours(args, rank, world, local_rank):
         "ms_median": round(float(np.median(ms)), 5), "ms_min": round(float(min(ms)), 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic (seeded, shapes of the paper's workloads)",
-        "config": {"workload": f"{wl.name}: B={s.B} H={s.H} N={s.N} M={s.M} D={s.D} {wl.dtype}"
-                               + ("" if args.variant == "flarepp" else f", {args.variant} mixer"),
+        "config": {"workload": workload_string(args.workload, args.variant),
                    "global_batch": s.B * world, "seq_len": s.N, "latents": s.M, "head_dim": s.D,
                    "heads": s.H, "parallelism": f"replicas x{world}" if world > 1 else "single",
                    "l2": "512 MB flush before every timed step"},
         "tflops": round(tflops, 3),
         "tensor_roofline_frac": round(tflops / peaks["bf16_tflops_sustained"], 4),
-        "roofline": roofline(costs, stage_ms, peaks, kind, clk.get("sm_mhz")),
+        "roofline": roofline(costs, stage_ms, peaks, kind, clk.get("sm_mhz"), sm_count(device)),
         "clocks": clk,
         "e2e": {"value": round(tokens / (e2e_max * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -512,7 +529,8 @@ def run_backward(args, rank, world, local_rank):
     tokens = s.tokens * world
     t = t_max * 1e-3
     flops = 24.0 * s.B * s.H * s.N * s.M * s.D
-    peak_tf = FP32_FMA_PER_CLK_PER_SM * 2 * SMS * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    sms = sm_count(device)
+    peak_tf = FP32_FMA_PER_CLK_PER_SM * 2 * sms * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
     ach = flops / t / 1e12
     return {
         "metric": "FLARE++ mixer backward tokens/s", "value": round(tokens / t, 1), "unit": UNIT,
@@ -525,7 +543,7 @@ def run_backward(args, rank, world, local_rank):
         "roofline": {"bound": "alu", "kernel": "backward passes (CUDA cores)", "achieved": round(ach, 3),
                      "peak": round(peak_tf, 3), "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4),
                      "traffic": None,
-                     "peak_source": "fp32 FMA: 128 lanes/clk/SM x 2 flops x 152 SMs x max SM clock"},
+                     "peak_source": f"fp32 FMA: 128 lanes/clk/SM x 2 flops x {sms} SMs x max SM clock"},
         "clocks": clk,
         "gpu_launches": 12 * args.steps,
         "impl": "ours",
@@ -596,22 +614,36 @@ class OraclePool:
         self.pool.join()
 
 
+def sample_tokens(pool, seconds: float) -> int:
+    """Tokens per (batch, head) problem such that one round of the pool (one
+    problem per process) takes about ``seconds``: whole problems where they
+    are that quick, else the first n tokens of each (at least 128)."""
+    s = pool.shape
+    probe = min(s.N, 2048)
+    t_probe = pool.round(probe)
+    if t_probe * s.N / probe <= seconds:
+        return s.N
+    return max(128, min(s.N, int(probe * seconds / max(t_probe, 1e-9))))
+
+
 def cpu_baseline(args):
     """The oracle's tokens/s on the host cores, on about ``--cpu-seconds`` of
-    whole-head problems of the benchmark workload."""
+    (batch, head) problems of the benchmark workload (each on its first n
+    tokens where whole problems would take longer than a third of that)."""
     cores = os.cpu_count() or 1
     pool = OraclePool(args.workload, cores, args.variant)
     s = pool.shape
+    n_tok = sample_tokens(pool, args.cpu_seconds / 3)
     done, el = 0, 0.0
     while el < args.cpu_seconds:
-        el += pool.round(s.N)
+        el += pool.round(n_tok)
         done += cores
     pool.close()
-    rate = done * s.N / s.H / el
+    rate = done * n_tok / s.H / el
     return {"value": round(rate, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} whole (batch, head) {args.variant} problems of {args.workload} (N={s.N}) in "
-                      f"{el:.1f} s on {cores} processes x 1 BLAS thread; tokens/s = "
-                      "problems x N / H / wall time"}
+            "sample": f"{done} (batch, head) {args.variant} problems of {args.workload} on the first "
+                      f"{n_tok} of N={s.N} tokens each, in {el:.1f} s on {cores} processes x 1 BLAS "
+                      "thread; tokens/s = problems x tokens / H / wall time"}
 
 
 def run_reference(args, rank, world):
@@ -623,11 +655,7 @@ def run_reference(args, rank, world):
     s = pool.shape
     budget = 120.0  # seconds for all warm-up and timed steps together
     per_step = max(0.05, budget / max(1, args.steps + args.warmup))
-    probe = min(s.N, 2048)
-    t_probe = pool.round(probe)
-    n_tok = s.N
-    if t_probe * s.N / probe > per_step:
-        n_tok = max(128, min(s.N, int(probe * per_step / t_probe)))
+    n_tok = sample_tokens(pool, per_step)
     times = []
     for i in range(args.warmup + args.steps):
         t = pool.round(n_tok)
@@ -640,8 +668,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, shapes of the paper's workloads)",
-            "config": {"workload": f"{args.workload}: B={s.B} H={s.H} N={s.N} M={s.M} D={s.D}"
-                                   + ("" if args.variant == "flarepp" else f", {args.variant} mixer"),
+            "config": {"workload": workload_string(args.workload, args.variant),
                        "parallelism": "host cores"},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores,
@@ -658,7 +685,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="pde2d", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--workload", default="aero", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--op", default="mixer", choices=["mixer", "project", "backward"],
                     help="what to time: the mixer forward, the fused token projections, or the "

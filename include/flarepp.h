@@ -106,8 +106,10 @@ flarepp_status_t flarepp_forward_debug(const void* K, const void* V, const void*
  * an allocation inside a timed loop.
  *   - Returns FLAREPP_ERR_NO_MEMORY when these sizes need more scratch than
  *     the 32 MiB maximum (flarepp_workspace_size(...) > 32 MiB).
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - Every call looks up the array's device address with the device current
+ *     (a lookup, no allocation). The first call on a device may also load the
+ *     library's device code there; make that first call before any stream
+ *     capture.
  *   - All calls on a device share the one array, and it keeps the previous
  *     call's contents (the library clears what must start at zero). Calls that
  *     overlap on the GPU — on different streams, or from different host threads
@@ -264,6 +266,30 @@ const char* flarepp_last_error(void);
  * log-sum-exp merge of Appendix B.2-B.3 is exact in exact arithmetic).
  */
 void flarepp_set_splits(int splits);
+
+/*
+ * Pipeline trace, for builds compiled with FLAREPP_TRACE (otherwise
+ * FLAREPP_ERR_UNSUPPORTED). pass 1 (synthesis), 2 (encode) or 3 (decode)
+ * arms the trace: block 0 of that pass records clock64 stamps of its
+ * pipeline events in the next calls; 0 disarms. When `host` is not NULL,
+ * up to n stamps (16 roles x 4096 events, role-major) are copied to it.
+ * Synchronous; not thread-safe: for profiling.
+ */
+flarepp_status_t flarepp_debug_trace(int pass, unsigned long long* host, int n);
+
+/*
+ * Test hook for the device-side failure path (the FLARE++ paper has no
+ * counterpart): while `pass` is 1 (synthesis), 2 (encode) or 3 (decode), the
+ * bf16 forward calls make one barrier of that pass expect an arrival that
+ * never comes, and every bounded wait of that pass gives up after about a
+ * millisecond instead of a second. The MMA-issuing thread waiting on the
+ * barrier gives up, records the timeout and makes its CTA leave;
+ * the call's output is then undefined and flarepp_sync_status returns
+ * FLAREPP_ERR_TIMEOUT. 0 (or any other value) switches it off. No fault,
+ * trap or unbounded wait is involved, and the context stays usable. Not
+ * thread-safe: for tests.
+ */
+void flarepp_test_fail_wait(int pass);
 
 /*
  * Measurement hook: while set (events != NULL, count >= 4), every forward call

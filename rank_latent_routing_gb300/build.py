@@ -16,7 +16,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-LIBDIR = os.path.join(PKG, "_lib")
+# FLAREPP_TRACE=1 selects the pipeline-trace build, kept in a folder of its own
+# so that it never stands in for the normal library
+TRACE = os.environ.get("FLAREPP_TRACE") == "1"
+LIBDIR = os.path.join(PKG, "_lib_trace" if TRACE else "_lib")
 LIB = os.path.join(LIBDIR, "libflarepp.so")
 SOURCES = ["flarepp.cu", "tc.cu", "proj.cu", "backward.cu", "flarepp_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -34,8 +37,9 @@ def nvcc() -> str:
 
 
 def _flags() -> list[str]:
+    trace = ["-DFLAREPP_TRACE"] if TRACE else []
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
-                   "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
+                   "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"] + trace
 
 
 def _deps() -> list[str]:

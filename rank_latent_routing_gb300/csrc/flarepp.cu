@@ -20,6 +20,7 @@ namespace flarepp {
 namespace {
 
 std::atomic<int> g_forced_splits{0};
+std::atomic<int> g_fail_wait{0};  // test hook: see flarepp_test_fail_wait
 thread_local char g_last_error[256] = "no error";
 cudaEvent_t* g_stage_events = nullptr;
 
@@ -192,6 +193,7 @@ flarepp_status_t launch_tc(const Problem& p, const Plan& pl, char* ws, cudaStrea
   dp.out = p.out;
   dp.B = p.B; dp.H = p.H; dp.N = p.N; dp.M = p.M; dp.D = p.D;
   dp.dbg_qd = p.dbg_qd; dp.dbg_q = p.dbg_q; dp.dbg_z = p.dbg_z; dp.dbg_l = p.dbg_l;
+  dp.fail_wait = g_fail_wait.load();
   TcWorkspace w{};
   w.part_z = reinterpret_cast<float*>(ws + pl.off_pz);
   w.part_l = reinterpret_cast<float*>(ws + pl.off_pl);
@@ -599,6 +601,14 @@ const char* flarepp_status_string(flarepp_status_t status) {
 const char* flarepp_last_error(void) { return flarepp::g_last_error; }
 
 void flarepp_set_splits(int splits) { flarepp::g_forced_splits.store(splits < 0 ? 0 : splits); }
+
+void flarepp_test_fail_wait(int pass) { flarepp::g_fail_wait.store(pass >= 1 && pass <= 3 ? pass : 0); }
+
+flarepp_status_t flarepp_debug_trace(int pass, unsigned long long* host, int n) {
+  const cudaError_t e = flarepp::tc_trace(pass, host, n);
+  if (e == cudaErrorNotSupported) return FLAREPP_ERR_UNSUPPORTED;
+  return flarepp::cuda_ok(e, "pipeline trace") ? FLAREPP_OK : FLAREPP_ERR_CUDA;
+}
 
 void flarepp_set_stage_events(cudaEvent_t* events, int count) {
   flarepp::g_stage_events = (events != nullptr && count >= 4) ? events : nullptr;

@@ -16,37 +16,29 @@
 // reads it.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "flarepp.h"
 
 namespace {
 
 // Largest scratch this entry point can use: 32 MiB per device.
 constexpr size_t kScratchBytes = size_t(32) << 20;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kScratchBytes];
 
-// Device address of g_static_scratch, looked up once per device (host code
-// must not use the symbol itself: on the host it names a stand-in object).
-std::mutex g_setup_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
+// Device address of g_static_scratch on the current device. Host code must
+// not use the symbol itself (on the host it names a stand-in object). The
+// address is looked up on every call, with the device current: the lookup
+// allocates nothing, and an address cached across calls would go stale when
+// the device's context is torn down and created again (cudaDeviceReset).
 flarepp_status_t scratch_for_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return FLAREPP_ERR_CUDA;
-  if (dev >= kMaxDevices) return FLAREPP_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return FLAREPP_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return FLAREPP_ERR_CUDA;
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return FLAREPP_OK;
 }
 

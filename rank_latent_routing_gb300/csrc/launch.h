@@ -34,6 +34,7 @@ struct DeviceProblem {
   float* dbg_q;
   float* dbg_z;
   float* dbg_l;
+  int fail_wait;       // test only: pass (1 synthesis, 2 encode, 3 decode) whose first P barrier never completes
 };
 
 // Split-N layout shared by the synthesis and encode passes: `tiles` blocks of
@@ -65,6 +66,7 @@ cudaError_t tc_forward(const DeviceProblem& p, const TcPlan& pl, const TcWorkspa
 // Reads and clears the tensor-core kernels' device error word (bit 0: a
 // bounded wait timed out).
 cudaError_t tc_take_error_word(unsigned* word);
+cudaError_t tc_trace(int pass, unsigned long long* host, int n);
 
 // ------------------------------------------------------ token projections
 constexpr int kMaxProjParts = 4;

@@ -73,6 +73,25 @@ using namespace sm100;
 
 __device__ unsigned g_tc_error = 0u;
 
+#ifdef FLAREPP_TRACE
+// Pipeline trace (trace builds only): clock64 stamps of block 0 of one pass,
+// g_trace[role][i]. g_trace_pass picks the pass: 1 synthesis, 2 encode (and
+// the simplified synthesis), 3 decode; 0 records nothing.
+constexpr int kTraceRoles = 16, kTraceLen = 4096;
+__device__ unsigned long long g_trace[kTraceRoles][kTraceLen];
+__device__ int g_trace_pass = 0;
+// roles: kernel start/end; TMA issue per tile; N0 per tile (4 parts);
+// issuing threads (slot, half) per step; softmax warps of the two halves
+// per (step, slot); epilogue phases
+enum : int { kTrStart = 0, kTrLoad = 1, kTrNorm = 2, kTrIssue = 6, kTrSoftmax = 10, kTrEpi = 12 };
+__device__ __forceinline__ void trace_stamp(bool on, int role, int i) {
+  if (on && i >= 0 && i < kTraceLen) g_trace[role][i] = clock64();
+}
+#define FLAREPP_TR(on, role, i) trace_stamp((on), (role), (i))
+#else
+#define FLAREPP_TR(on, role, i) ((void)0)
+#endif
+
 constexpr int kThreads = 512;
 constexpr int kWarpIssue = 1;        // first MMA-issuing warp: warp 1 + 2k + hf
 constexpr int kWarpNorm = 5;         // N0 of the synthesis tiles: warps 0, 5, 14 and 15
@@ -84,6 +103,9 @@ constexpr uint32_t kSlotCols = 256;  // slot s starts at column 256*s
 constexpr uint32_t kColO = 128;      // accumulator of column half 0; half 1's follows it
 constexpr uint32_t kColQ = 224;      // the slot's latent queries (bf16 pairs), A operand of the scores
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
+// under the test hook that makes one barrier never complete, waits give up
+// after ~1 ms, so that the forced timeout ends the call quickly
+constexpr long long kTestWaitLimit = 2000000LL;
 
 // How the two TMEM slots of a split-kernel CTA divide the work:
 //  kLanes   (M <= 64)  each slot holds the latents twice; lanes 0-63 and 64-127
@@ -102,6 +124,7 @@ struct Shared {
   uint64_t o_full[2][2];  // the last products of half h of slot k done
   uint64_t q_tmem;        // the latent queries are in TMEM
   uint64_t drain;         // every MMA of the CTA has completed
+  long long wait_limit;   // clock cycles a wait may take before it gives up
   uint32_t tmem_base;
   int abort;
   int last;
@@ -112,7 +135,7 @@ struct Shared {
 __device__ __forceinline__ bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   if (*(volatile int*)&sh.abort) return false;
-  if (mbar_wait(bar, parity, kWaitLimit)) return true;
+  if (mbar_wait(bar, parity, sh.wait_limit)) return true;
   atomicOr(&g_tc_error, kErrTimeout);
   *(volatile int*)&sh.abort = 1;
   return false;
@@ -344,6 +367,7 @@ struct SplitParams {
   __nv_bfloat16* out;       // gated: Q; encode: Z ([BH][M][D])
   float* dbg_a;             // gated: Qd; encode: Z (as rounded)
   float* dbg_b;             // gated: Q (as rounded); encode: L
+  int fail_wait;            // test only: P barrier of slot 0, half 0 expects one arrival too many
 };
 
 struct SlotPlan {
@@ -435,11 +459,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < 2; ++k)
       for (int hf = 0; hf < 2; ++hf) {
         mbar_init(&sh.s_full[k][hf], 1);
-        mbar_init(&sh.p_full[k][hf], 4);  // one arrival per softmax warp of the half
+        // one arrival per softmax warp of the half (one more under the test hook)
+        mbar_init(&sh.p_full[k][hf], 4 + (p.fail_wait && k == 0 && hf == 0 ? 1 : 0));
         mbar_init(&sh.o_full[k][hf], 1);
       }
     mbar_init(&sh.drain, 4);
     mbar_init(&sh.q_tmem, 4);
+    sh.wait_limit = p.fail_wait ? kTestWaitLimit : kWaitLimit;
     sh.abort = 0;
     sh.last = 0;
     fence_mbar_init();
@@ -454,6 +480,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
+#ifdef FLAREPP_TRACE
+  const bool tr_on = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
+                     g_trace_pass == (kKind == kPassEncode ? 2 : 1);
+#endif
+  FLAREPP_TR(tr_on && threadIdx.x == 0, kTrStart, 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -492,19 +523,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(dst, &tm_k, &sh.full[s], 0, n_begin + t * kTile, bh);
           if (kSepValues) tma_load_3d(dst + kValueOff, &tm_v, &sh.full[s], 0, n_begin + t * kTile, bh);
           issued = t + 1;
+          FLAREPP_TR(tr_on, kTrLoad, t);
         }
       }
       if (kNormKeys) {
         ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
         const int tn = t - kLag;
-        if (ok && tn >= 0) ok = normalise_part<D, kStages>(sh, sStage, kStageBytes, tn, 0, lane);
+        if (ok && tn >= 0) {
+          ok = normalise_part<D, kStages>(sh, sStage, kStageBytes, tn, 0, lane);
+          FLAREPP_TR(tr_on && ok && lane == 0, kTrNorm, tn);
+        }
       }
     }
     if (lane == 0 && *(volatile int*)&sh.abort) {
       // let the copies still in flight land before the CTA leaves
       for (int t = max(0, issued - kStages); t < issued; ++t)
-        mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, kWaitLimit);
-      mbar_wait(&sh.q_full, 0, kWaitLimit);
+        mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, sh.wait_limit);
+      mbar_wait(&sh.q_full, 0, sh.wait_limit);
     }
   } else if (warp < kWarpNorm) {
     // ---------------------------------- MMA of column half hf of slot kk
@@ -602,21 +637,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = issue_s(t0);
       for (int j = 0, t = t0; ok && j < nsteps; ++j, t += dt) {
         if (!wait_or_abort(sh, &sh.p_full[kk][hf], j & 1)) break;
+        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * j);
         tc_fence_after();
         issue_pv(t, j > 0 ? 1u : 0u);
         release(t);
+        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * j + 1);
         if (j + 1 < nsteps) ok = issue_s(t + dt);
+        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * j + 2);
       }
       // every MMA of this CTA completes before TMEM is released
       mma_commit(&sh.drain);
-      mbar_wait(&sh.drain, 0, kWaitLimit);
+      mbar_wait(&sh.drain, 0, sh.wait_limit);
     }
   } else if (warp == kWarpNorm || warp >= kWarpSoftmax + 8) {
     // ------------------------------------------- N0 of the synthesis keys
     if (kNormKeys) {
       const int part = warp == kWarpNorm ? 1 : warp - (kWarpSoftmax + 6);  // 1, 2, 3
-      for (int t = 0; t < T; ++t)
+      for (int t = 0; t < T; ++t) {
         if (!normalise_part<D, kStages>(sh, sStage, kStageBytes, t, part, lane)) break;
+        FLAREPP_TR(tr_on && lane == 0, kTrNorm + part, t);
+      }
     }
   } else if (warp >= kWarpSoftmax && warp < kWarpSoftmax + 8) {
     // ------------------------------------------------- softmax + epilogue
@@ -626,6 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const int lanes_half = sp.mode == kLanes ? (row >> 6) : 0;
     const float c = rsqrtf((float)D) * kLog2e;
+#ifdef FLAREPP_TRACE
+    const bool tr_sm = tr_on && lane == 0 && (warp == kWarpSoftmax || warp == kWarpSoftmax + 4);
+#endif
     float r[2] = {-INFINITY, -INFINITY}, ro[2] = {-INFINITY, -INFINITY};  // references of P and of O
     bool acc[2] = {false, false};
     bool ok = true;
@@ -658,6 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_base + k * kSlotCols + 64 * hf;
         const uint32_t tO = tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo;
         if (!wait_or_abort(sh, &sh.s_full[k][hf], j & 1)) { ok = false; continue; }
+        FLAREPP_TR(tr_sm, kTrSoftmax + hf, 4 * j + 2 * k);
         tc_fence_after();
         const int t = slot_tile(sp, k, j) + lanes_half;
         bool wrote = false;
@@ -675,6 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         finish_half<D>(&sh.p_full[k][hf], tO, r[k], ro[k], acc[k]);
+        FLAREPP_TR(tr_sm, kTrSoftmax + hf, 4 * j + 2 * k + 1);
         if (wrote) acc[k] = true;
       }
     }
@@ -682,6 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // scratch below
     if (ok) ok = wait_or_abort(sh, &sh.drain, 0);
     tc_fence_after();
+    FLAREPP_TR(tr_on && tid == 0, kTrEpi, 0);
 
     // 1) each softmax stream's (L, Z) into shared memory: stream e =
     //    256 hf + 128 k + row
@@ -736,11 +782,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     softmax_groups_sync();
     const size_t grp = (size_t)bh * gridDim.y + group;
+    FLAREPP_TR(tr_on && tid == 0, kTrEpi, 1);
     if (tid == 0) {
       const unsigned prev = atomicAdd(p.counters + grp, 1u);
       sh.last = prev == (unsigned)(p.splits - 1);
     }
     softmax_groups_sync();
+    FLAREPP_TR(tr_on && tid == 0, kTrEpi, 2);
     if (sh.last) {
       __threadfence();
       if (tid == 0) p.counters[grp] = 0u;  // ready for the next call
@@ -828,6 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FLAREPP_TR(tr_on && threadIdx.x == 0, kTrStart, 1);
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -839,6 +888,7 @@ struct DecodeParams {
   int heads;           // Q/Z slots in shared memory: the most heads one CTA's tiles span
   int q_by_head;       // routing queries [H][M][D] (1) or [BH][M][D] (0)
   __nv_bfloat16* out;  // [BH][N][D]
+  int fail_wait;       // test only: P barrier of slot 0, half 0 expects one arrival too many
 };
 
 // Token-tile ring depth of the decode kernel: a compile-time constant, so
@@ -929,10 +979,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < 2; ++k)
       for (int hf = 0; hf < 2; ++hf) {
         mbar_init(&sh.s_full[k][hf], 1);
-        mbar_init(&sh.p_full[k][hf], 4);
+        mbar_init(&sh.p_full[k][hf], 4 + (p.fail_wait && k == 0 && hf == 0 ? 1 : 0));
         mbar_init(&sh.o_full[k][hf], 1);
       }
     mbar_init(&sh.drain, 4);
+    sh.wait_limit = p.fail_wait ? kTestWaitLimit : kWaitLimit;
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -946,6 +997,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
+#ifdef FLAREPP_TRACE
+  const bool tr_on = blockIdx.x == 0 && g_trace_pass == 3;
+#endif
+  FLAREPP_TR(tr_on && threadIdx.x == 0, kTrStart, 0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -969,11 +1024,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&sh.full[s], L::kTileBytes);
         tma_load_3d(sK + s * L::kTileBytes, &tm_k, &sh.full[s], 0, (first + t - hs * n_tiles) * kTile, h0 + hs);
         issued = t + 1;
+        FLAREPP_TR(tr_on, kTrLoad, t);
       }
       if (*(volatile int*)&sh.abort) {
         for (int t = max(0, issued - stages); t < issued; ++t)
-          mbar_wait(&sh.full[t % stages], (t / stages) & 1, kWaitLimit);
-        mbar_wait(&sh.q_full, 0, kWaitLimit);
+          mbar_wait(&sh.full[t % stages], (t / stages) & 1, sh.wait_limit);
+        mbar_wait(&sh.q_full, 0, sh.wait_limit);
       }
     }
   } else if (warp < kWarpNorm) {
@@ -1030,8 +1086,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = issue_s(t, b, hoff);
       for (int u = 0; ok && u < nsteps; ++u) {
         if (!wait_or_abort(sh, &sh.p_full[kk][hf], u & 1)) break;
+        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * u);
         tc_fence_after();
         issue_pv(t, b, hoff);
+        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * u + 1);
         if (++b == nsub) {
           b = 0;
           t += 4;
@@ -1039,9 +1097,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (u + 1 < nsteps) ok = issue_s(t, b, hoff);
         else mma_commit(&sh.o_full[kk][hf]);
+        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * u + 2);
       }
       mma_commit(&sh.drain);
-      mbar_wait(&sh.drain, 0, kWaitLimit);
+      mbar_wait(&sh.drain, 0, sh.wait_limit);
     }
   } else if (warp >= kWarpSoftmax && warp < kWarpSoftmax + 8) {
     const int tid = threadIdx.x - 32 * kWarpSoftmax;  // 0..255
@@ -1049,6 +1108,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const float c = rsqrtf((float)D) * kLog2e;
+#ifdef FLAREPP_TRACE
+    const bool tr_sm = tr_on && lane == 0 && (warp == kWarpSoftmax || warp == kWarpSoftmax + 4);
+#endif
     float r[2] = {-INFINITY, -INFINITY}, ro[2] = {-INFINITY, -INFINITY};
     bool acc[2] = {false, false};
     // out = O / rowsum of this half's accumulator, for its own token tile t
@@ -1076,6 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_base + k * kSlotCols + 64 * hf;
         const uint32_t tO = tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo;
         ok = ok && wait_or_abort(sh, &sh.s_full[k][hf], u & 1);
+        FLAREPP_TR(tr_sm, kTrSoftmax + hf, 4 * u + 2 * k);
         tc_fence_after();
         if (b == 0) {
           // the previous tile's products are in: its output goes out before
@@ -1088,6 +1151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int valid = tk[k] < T ? min(64, p.M - 64 * b) : 0;
         if (valid > 0) softmax_half(tS, valid, c, r[k]);
         finish_half<D>(&sh.p_full[k][hf], tO, r[k], ro[k], acc[k]);
+        FLAREPP_TR(tr_sm, kTrSoftmax + hf, 4 * u + 2 * k + 1);
         if (valid > 0) acc[k] = true;
       }
       if (++b == nsub) {
@@ -1108,6 +1172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FLAREPP_TR(tr_on && threadIdx.x == 0, kTrStart, 1);
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -1166,6 +1231,7 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
   const dim3 grid(pl.splits, pl.qgroups, BH);
   SplitParams sp{};
   sp.N = pr.N; sp.M = pr.M; sp.H = pr.H;
+  sp.fail_wait = 0;
   sp.qtiles = pl.tiles; sp.splits = pl.splits; sp.split_len = pl.split_len;
   sp.part_z = ws.part_z; sp.part_l = ws.part_l;
 
@@ -1176,6 +1242,7 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
     a.counters = ws.counters;
     a.q_by_head = 1;
     a.out = static_cast<__nv_bfloat16*>(ws.q);
+    a.fail_wait = pr.fail_wait == 1;
     if (pr.variant == kVariantSimplified) {
       a.dbg_a = pr.dbg_q;  // Q = Qd, as rounded
       e = launch_split<D, kPassEncode>(m_seed, m_ks, m_vs, a, grid, stream, "launch synthesis", failed);
@@ -1196,6 +1263,7 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
     SplitParams a = sp;
     a.counters = ws.counters + (size_t)BH * pl.qgroups;
     a.q_by_head = flare ? 1 : 0;
+    a.fail_wait = pr.fail_wait == 2;
     a.out = static_cast<__nv_bfloat16*>(ws.z);
     a.dbg_a = pr.dbg_z;
     a.dbg_b = pr.dbg_l;
@@ -1212,6 +1280,7 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
     d.heads = pl.decode_heads;
     d.q_by_head = flare ? 1 : 0;
     d.out = static_cast<__nv_bfloat16*>(pr.out);
+    d.fail_wait = pr.fail_wait == 3;
     const size_t smem = decode_smem<D>(pr.M, pl.decode_heads);
     *failed = "cudaFuncSetAttribute(decode)";
     if ((e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
@@ -1290,6 +1359,29 @@ cudaError_t tc_forward(const DeviceProblem& p, const TcPlan& pl, const TcWorkspa
                        cudaStream_t stream, const char** failed_call) {
   return p.D == 16 ? tc::forward_d<16>(p, pl, ws, events, stream, failed_call)
                    : tc::forward_d<32>(p, pl, ws, events, stream, failed_call);
+}
+
+// Pipeline trace (trace builds): pass > 0 arms block 0 of that pass and
+// clears the stamps, pass == 0 disarms; `host`, when given, receives up to
+// n stamps ([role][index] order). Without FLAREPP_TRACE: unsupported.
+cudaError_t tc_trace(int pass, unsigned long long* host, int n) {
+#ifdef FLAREPP_TRACE
+  cudaError_t e = cudaMemcpyToSymbol(tc::g_trace_pass, &pass, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (pass > 0) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, tc::g_trace)) != cudaSuccess) return e;
+    if ((e = cudaMemset(p, 0, sizeof(tc::g_trace))) != cudaSuccess) return e;
+  }
+  if (host != nullptr && n > 0) {
+    const size_t bytes = std::min(sizeof(tc::g_trace), (size_t)n * sizeof(unsigned long long));
+    if ((e = cudaMemcpyFromSymbol(host, tc::g_trace, bytes)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+#else
+  (void)pass; (void)host; (void)n;
+  return cudaErrorNotSupported;
+#endif
 }
 
 cudaError_t tc_take_error_word(unsigned* word) {

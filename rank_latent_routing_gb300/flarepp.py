@@ -76,6 +76,8 @@ def _load() -> ctypes.CDLL:
     lib.flarepp_set_stage_events.restype = None
     lib.flarepp_plan_info.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int), i]
     lib.flarepp_plan_info.restype = ctypes.c_int
+    lib.flarepp_test_fail_wait.argtypes = [i]
+    lib.flarepp_test_fail_wait.restype = None
     return lib
 
 
@@ -129,6 +131,7 @@ def _check(K, V, Ks_raw, Qseed, Qf, gate):
 def forward(K, V, Ks_raw, Qseed, Qf, gate, out=None, stream=None):
     """The FLARE++ mixer forward; returns ``out`` [B,H,N,D] (allocated if None)."""
     B, H, N, M, D, code = _check(K, V, Ks_raw, Qseed, Qf, gate)
+    _check_tensors(K, [("out", out, (B, H, N, D), False)])
     if out is None:
         out = torch.empty_like(K)
     with torch.cuda.device(K.device):
@@ -148,6 +151,7 @@ def workspace_size(B, H, N, M, D, dtype=torch.bfloat16, device=None) -> int:
 def forward_ws(K, V, Ks_raw, Qseed, Qf, gate, workspace, out=None, stream=None):
     """As ``forward`` with a caller-owned workspace (uint8 CUDA tensor)."""
     B, H, N, M, D, code = _check(K, V, Ks_raw, Qseed, Qf, gate)
+    _check_tensors(K, [("out", out, (B, H, N, D), False)])
     if out is None:
         out = torch.empty_like(K)
     with torch.cuda.device(K.device):
@@ -165,6 +169,9 @@ def forward_static(K, V, Ks_raw, Qseed, Qf, gate, out, stream=None):
     comes from a fixed 32 MiB array inside the library and ``out`` must be
     given. Calls that overlap on the GPU share that array and race."""
     B, H, N, M, D, code = _check(K, V, Ks_raw, Qseed, Qf, gate)
+    if out is None:
+        raise ValueError("forward_static writes into a caller-given out (it allocates nothing)")
+    _check_tensors(K, [("out", out, (B, H, N, D), False)])
     with torch.cuda.device(K.device):
         rc = _lib.flarepp_forward_static(_ptr(K), _ptr(V), _ptr(Ks_raw), _ptr(Qseed), _ptr(Qf),
                                          _ptr(gate), B, H, N, M, D, code, _ptr(out),
@@ -336,6 +343,13 @@ def sync_status(stream=None) -> int:
 def set_splits(splits: int) -> None:
     """Test hook: force the token split count (0 = automatic)."""
     _lib.flarepp_set_splits(int(splits))
+
+
+def test_fail_wait(pass_id: int) -> None:
+    """Test hook: make one barrier of pass 1 (synthesis), 2 (encode) or 3
+    (decode) of the next bf16 forward calls never complete, so that the call
+    ends with a recorded timeout; 0 switches it off."""
+    _lib.flarepp_test_fail_wait(int(pass_id))
 
 
 PLAN_FIELDS = ("splits", "split_len", "latent_groups", "decode_tiles_per_cta",
