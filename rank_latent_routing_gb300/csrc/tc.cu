@@ -132,13 +132,25 @@ struct Shared {
 
 // A phase that has completed is taken at once; the abort flag is read only on
 // the slow path, so a wait that needs no waiting costs no shared-memory load.
+// kSleep: the thread sleeps in the barrier between tests (for long,
+// latency-tolerant waits: a producer a ring ahead) instead of polling, which
+// would take issue slots from the warps beside it.
+template <bool kSleep = false>
 __device__ __forceinline__ bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   if (*(volatile int*)&sh.abort) return false;
-  if (mbar_wait(bar, parity, sh.wait_limit)) return true;
+  if (kSleep ? mbar_wait_sleep(bar, parity, sh.wait_limit) : mbar_wait(bar, parity, sh.wait_limit)) return true;
   atomicOr(&g_tc_error, kErrTimeout);
   *(volatile int*)&sh.abort = 1;
   return false;
+}
+
+// wait_or_abort by every lane of a convergent warp; the warp agrees on the
+// outcome (a lane that gave up makes the whole warp give up), so that the
+// warp stays convergent for the elect.sync-issued MMAs that follow.
+__device__ __forceinline__ bool warp_wait(Shared& sh, uint64_t* bar, uint32_t parity) {
+  const bool ok = wait_or_abort(sh, bar, parity);
+  return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // One arrival per warp: the lanes' TMEM accesses are ordered before the
@@ -515,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < T + kLag; ++t) {
       if (lane == 0 && ok && t < T) {
         const int s = t % kStages;
-        if (t >= kStages && !wait_or_abort(sh, &sh.empty[s], ((t / kStages) - 1) & 1)) {
+        if (t >= kStages && !wait_or_abort<true>(sh, &sh.empty[s], ((t / kStages) - 1) & 1)) {
           ok = false;
         } else {
           unsigned char* dst = sStage + s * kStageBytes;
@@ -543,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kWarpNorm) {
     // ---------------------------------- MMA of column half hf of slot kk
-    if (lane == 0) {
+    {  // the whole warp runs the issuing loop; one elected lane issues
       const int kk = (warp - kWarpIssue) >> 1, hf = (warp - kWarpIssue) & 1;
       const uint32_t aOnes = smem_u32(sOnes);
       const uint32_t idS = idesc_bf16(128, 64, false, false);
@@ -563,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dO = tmem + kk * kSlotCols + kColO + hf * L::kNo;
       const uint32_t aP = tmem + kk * kSlotCols + 64 * hf;
       auto ready = [&](int t) -> bool {
-        return wait_or_abort(sh, kNormKeys ? &sh.norm[t % kStages] : &sh.full[t % kStages], (t / kStages) & 1);
+        return warp_wait(sh, kNormKeys ? &sh.norm[t % kStages] : &sh.full[t % kStages], (t / kStages) & 1);
       };
       // Descriptors of stage 0, built once; stage s is s * kStageBytes further:
       // the key descriptor's start address moves by that much, and so does the
@@ -579,29 +591,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       // scores of the half's 64 token columns of tile t (and t + 1 in the
       // lanes mode); the latent queries (A) are read from TMEM, the keys (B)
       // from the staged tile
-      auto issue_s = [&](int t) -> bool {
+      // tile t (and t + 1 in the lanes mode) staged and normalised; waited
+      // for while the issuer has nothing else to do
+      auto tile_ready = [&](int t) -> bool {
         if (!ready(t)) return false;
+        return !(lanes && t + 1 < T) || ready(t + 1);
+      };
+      auto issue_s = [&](int t) -> bool {
         if (lanes) {
           const bool has_b = t + 1 < T;
-          if (has_b && !ready(t + 1)) return false;
           tc_fence_after();
           const uint64_t ka = key_desc(t);
 #pragma unroll
           for (int q = 0; q < D / 16; ++q)
-            mma_ts_masked(dS, tQ + q * 8, L::adv(ka, 32 * q), idS, q > 0, kLo, kLo, kAll, kAll);
+            mma_ts_masked_elect(dS, tQ + q * 8, L::adv(ka, 32 * q), idS, q > 0, kLo, kLo, kAll, kAll);
           if (has_b) {
             const uint64_t kb = key_desc(t + 1);
 #pragma unroll
             for (int q = 0; q < D / 16; ++q)
-              mma_ts_masked(dS, tQ + q * 8, L::adv(kb, 32 * q), idS, q > 0, kAll, kAll, kLo, kLo);
+              mma_ts_masked_elect(dS, tQ + q * 8, L::adv(kb, 32 * q), idS, q > 0, kAll, kAll, kLo, kLo);
           }
         } else {
           tc_fence_after();
           const uint64_t ka = key_desc(t);
 #pragma unroll
-          for (int q = 0; q < D / 16; ++q) mma_ts(dS, tQ + q * 8, L::adv(ka, 32 * q), idS, q > 0);
+          for (int q = 0; q < D / 16; ++q) mma_ts_elect(dS, tQ + q * 8, L::adv(ka, 32 * q), idS, q > 0);
         }
-        mma_commit(&sh.s_full[kk][hf]);
+        mma_commit_elect(&sh.s_full[kk][hf]);
         return true;
       };
       // O_hf (+)= P_hf [V | 1]_hf for tile t (and t + 1): slices 4hf .. 4hf+3
@@ -612,41 +628,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool has_b = t + 1 < T;
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            mma_ts_masked(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kLo, kLo, kAll,
+            mma_ts_masked_elect(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kLo, kLo, kAll,
                           kAll);
           if (has_b) {
             const uint64_t vb = val_desc(t + 1);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              mma_ts_masked(dO, aP + i * 8, L::adv(vb, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kAll, kAll, kLo,
+              mma_ts_masked_elect(dO, aP + i * 8, L::adv(vb, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kAll, kAll, kLo,
                             kLo);
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) mma_ts(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
+          for (int i = 0; i < 4; ++i) mma_ts_elect(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
         }
       };
       // the stage(s) of tile t can be refilled once this thread's products of
       // them are done (every issuing thread that read them releases)
       auto release = [&](int t) {
-        mma_commit(&sh.empty[t % kStages]);
-        if (lanes && t + 1 < T) mma_commit(&sh.empty[(t + 1) % kStages]);
+        mma_commit_elect(&sh.empty[t % kStages]);
+        if (lanes && t + 1 < T) mma_commit_elect(&sh.empty[(t + 1) % kStages]);
       };
-      bool ok = nsteps > 0 && wait_or_abort(sh, &sh.q_tmem, 0);
+      bool ok = nsteps > 0 && warp_wait(sh, &sh.q_tmem, 0) && tile_ready(t0);
       tc_fence_after();
       if (ok) ok = issue_s(t0);
+      // Per step: the products that read P, then at once the next step's
+      // scores (its tile was waited for before P was), then the release of
+      // the tile: the path from P to the next scores holds no wait and one
+      // commit.
       for (int j = 0, t = t0; ok && j < nsteps; ++j, t += dt) {
-        if (!wait_or_abort(sh, &sh.p_full[kk][hf], j & 1)) break;
-        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * j);
+        const bool more = j + 1 < nsteps;
+        if (more && !tile_ready(t + dt)) break;
+        if (!warp_wait(sh, &sh.p_full[kk][hf], j & 1)) break;
+        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * j);
         tc_fence_after();
         issue_pv(t, j > 0 ? 1u : 0u);
+        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * j + 1);
+        if (more) ok = issue_s(t + dt);
         release(t);
-        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * j + 1);
-        if (j + 1 < nsteps) ok = issue_s(t + dt);
-        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * j + 2);
+        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * j + 2);
       }
       // every MMA of this CTA completes before TMEM is released
-      mma_commit(&sh.drain);
+      mma_commit_elect(&sh.drain);
       mbar_wait(&sh.drain, 0, sh.wait_limit);
     }
   } else if (warp == kWarpNorm || warp >= kWarpSoftmax + 8) {
@@ -1019,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int t = 0; t < T; ++t) {
         const int s = t % stages;
-        if (t >= stages && !wait_or_abort(sh, &sh.empty[s], ((t / stages) - 1) & 1)) break;
+        if (t >= stages && !wait_or_abort<true>(sh, &sh.empty[s], ((t / stages) - 1) & 1)) break;
         const int hs = head_slot(t);
         mbar_arrive_expect_tx(&sh.full[s], L::kTileBytes);
         tma_load_3d(sK + s * L::kTileBytes, &tm_k, &sh.full[s], 0, (first + t - hs * n_tiles) * kTile, h0 + hs);
@@ -1033,7 +1055,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < kWarpNorm) {
-    if (lane == 0) {
+    {  // the whole warp runs the issuing loop; one elected lane issues
       const int kk = (warp - kWarpIssue) >> 1, hf = (warp - kWarpIssue) & 1;
       const uint32_t aZ = smem_u32(sZ), aOnes = smem_u32(sOnes);
       const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
@@ -1047,21 +1069,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dO = tmem + kk * kSlotCols + kColO + hf * L::kNo;
       // scores of local tile t against routes 64b .. 64b+63 of its head, whose
       // Q and Z sit `hoff` bytes into their arrays
+      // the K tile of local tile t staged (waited for at its first route
+      // block, while the issuer has nothing else to do)
+      auto tile_wait = [&](int t, int b) -> bool {
+        if (t >= T || b != 0) return true;
+        return warp_wait(sh, &sh.full[t % stages], (t / stages) & 1);
+      };
       auto issue_s = [&](int t, int b, uint32_t hoff) -> bool {
         if (t < T) {
           const int s = t % stages;
-          if (b == 0) {
-            if (!wait_or_abort(sh, &sh.full[s], (t / stages) & 1)) return false;
-            tc_fence_after();
-          }
+          tc_fence_after();
           const int width = min(64, p.M - 64 * b);
           const uint64_t a = L::adv(dK0, s * L::kTileBytes), bq = L::adv(dQ0, hoff + b * 64 * L::kRowBytes);
           const uint32_t id = width >= 64 ? idS64 : idesc_bf16(128, width, false, false);
 #pragma unroll
-          for (int q = 0; q < D / 16; ++q) mma_ss(dS, L::adv(a, 32 * q), L::adv(bq, 32 * q), id, q > 0);
-          if (b == nsub - 1) mma_commit(&sh.empty[s]);
+          for (int q = 0; q < D / 16; ++q) mma_ss_elect(dS, L::adv(a, 32 * q), L::adv(bq, 32 * q), id, q > 0);
         }
-        mma_commit(&sh.s_full[kk][hf]);
+        mma_commit_elect(&sh.s_full[kk][hf]);
+        // the tile's last read: its stage may be refilled
+        if (t < T && b == nsub - 1) mma_commit_elect(&sh.empty[t % stages]);
         return true;
       };
       // O_hf (+)= P_hf [Z | 1] over the route slices of block b
@@ -1073,33 +1099,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t first = b > 0 ? 1u : 0u;
         if (nsl == 4) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) mma_ts(dO, aP + i * 8, L::adv(v, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
+          for (int i = 0; i < 4; ++i) mma_ts_elect(dO, aP + i * 8, L::adv(v, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
         } else {
-          for (int i = 0; i < nsl; ++i) mma_ts(dO, aP + i * 8, L::adv(v, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
+          for (int i = 0; i < nsl; ++i) mma_ts_elect(dO, aP + i * 8, L::adv(v, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
         }
       };
       // the step's tile and route block, advanced without a division
       int t = tile_of(kk, 0, hf), b = 0;
       uint32_t hoff = head_slot(t) * head_bytes;
       const int nsteps = kk ? steps[1] : steps[0];  // no run-time array index: steps stays in registers
-      bool ok = nsteps > 0 && wait_or_abort(sh, &sh.q_full, 0);
+      bool ok = nsteps > 0 && warp_wait(sh, &sh.q_full, 0) && tile_wait(t, b);
       if (ok) ok = issue_s(t, b, hoff);
+      // Per step: the products that read P, then at once the next step's
+      // scores (whose tile was waited for before P was).
       for (int u = 0; ok && u < nsteps; ++u) {
-        if (!wait_or_abort(sh, &sh.p_full[kk][hf], u & 1)) break;
-        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * u);
+        int tn = t, bn = b + 1;
+        uint32_t hn = hoff;
+        if (bn == nsub) {
+          bn = 0;
+          tn = t + 4;
+          hn = head_slot(tn) * head_bytes;
+        }
+        const bool more = u + 1 < nsteps;
+        if (more && !tile_wait(tn, bn)) break;
+        if (!warp_wait(sh, &sh.p_full[kk][hf], u & 1)) break;
+        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * u);
         tc_fence_after();
         issue_pv(t, b, hoff);
-        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * u + 1);
-        if (++b == nsub) {
-          b = 0;
-          t += 4;
-          hoff = head_slot(t) * head_bytes;
-        }
-        if (u + 1 < nsteps) ok = issue_s(t, b, hoff);
-        else mma_commit(&sh.o_full[kk][hf]);
-        FLAREPP_TR(tr_on, kTrIssue + 2 * kk + hf, 3 * u + 2);
+        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * u + 1);
+        if (more) ok = issue_s(tn, bn, hn);
+        else mma_commit_elect(&sh.o_full[kk][hf]);
+        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * u + 2);
+        t = tn;
+        b = bn;
+        hoff = hn;
       }
-      mma_commit(&sh.drain);
+      mma_commit_elect(&sh.drain);
       mbar_wait(&sh.drain, 0, sh.wait_limit);
     }
   } else if (warp >= kWarpSoftmax && warp < kWarpSoftmax + 8) {

@@ -85,6 +85,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="pde2d")
     ap.add_argument("--mhz", type=float, default=2070.0, help="SM clock for the microsecond column")
+    ap.add_argument("--save", default=None, help="write the raw stamps of each pass to <save>_<pass>.npy")
     args = ap.parse_args()
     if os.environ.get("FLAREPP_TRACE") != "1":
         raise SystemExit("set FLAREPP_TRACE=1: the trace needs a trace build of the library")
@@ -116,7 +117,10 @@ def main():
         buf = (ctypes.c_ulonglong * (ROLES * LEN))()
         if lib.flarepp_debug_trace(0, buf, ROLES * LEN) != 0:
             raise SystemExit("reading the trace failed")
-        report(name, np.frombuffer(buf, dtype=np.uint64).astype(np.int64).reshape(ROLES, LEN), args.mhz)
+        st = np.frombuffer(buf, dtype=np.uint64).astype(np.int64).reshape(ROLES, LEN)
+        if args.save:
+            np.save(f"{args.save}_{name}.npy", st)
+        report(name, st, args.mhz)
     if flarepp.sync_status() != 0:
         raise SystemExit("device error during the traced calls")
 
