@@ -39,7 +39,7 @@ struct DeviceProblem {
 
 // Split-N layout shared by the synthesis and encode passes: `tiles` blocks of
 // (up to) 128 latent rows per head, handled by `qgroups` CTAs per token split
-// (two blocks per CTA when M > 128); `splits` token ranges of `split_len`
+// (one block per CTA); `splits` token ranges of `split_len`
 // tokens (a multiple of 128); `streams` partial results per (block, split,
 // row): 1, the token streams inside a CTA being merged before the write.
 struct TcPlan {

@@ -4,51 +4,52 @@
 // Two kernels carry the three attention calls of the mixer (FLARE++ paper,
 // Section 3.2 eq. 6 and eq. 8):
 //
-//  * split_kernel — latent queries attend over one token range (split) of a
-//    head. Scores S = Q K^T land in TMEM; threads run an online softmax over
-//    the tokens; P goes back to TMEM in bf16 over the scores and the tensor
-//    core accumulates O += P [V | 1] in TMEM, the appended ones column giving
-//    the softmax row sum. Each split's (Z_s, L_s) goes to global memory and
-//    the last CTA of a head to arrive merges all splits with the stable
-//    log-sum-exp schedule of Appendix B.3 (eq. 29-33). The synthesis instance
+//  * split_kernel — a block of up to 128 latent queries attends over one
+//    token range (split) of a head. Scores S = Q K^T land in TMEM; threads
+//    run an online softmax over the tokens; P goes back to TMEM in bf16 over
+//    the second half of the scores and the tensor core accumulates O += P [V | 1] in TMEM, the
+//    appended ones column giving the softmax row sum. Each split's (Z_s, L_s)
+//    goes to global memory and the last CTA of a head to arrive merges all
+//    splits with the stable log-sum-exp schedule of Appendix B.3 (eq. 29-33);
+//    a head with one split writes its result directly. The synthesis instance
 //    normalises each staged Ks_raw tile in place (N0, eq. 5), uses it as both
 //    keys and values (eq. 19) and ends with the gate (eq. 7):
 //    Q = N0(Qf) + g * Qd in fp32, cast to bf16. The encode instance ends with
 //    Z (bf16) and L.
 //  * decode_kernel — tokens attend over the M routes: Q and Z of the head stay
-//    in shared memory for all of the CTA's token tiles; each column half of a
-//    TMEM slot owns a token tile and computes S = K Q^T 64 routes at a time
-//    with an online softmax over M per token, and O += P [Z | 1];
-//    out = O / rowsum in bf16.
+//    in shared memory for all of the CTA's token tiles; a token tile's scores
+//    S = K Q^T are taken 64 routes at a time with an online softmax over M per
+//    token, and O += P [Z | 1]; out = O / rowsum in bf16.
 //
-// One CTA per SM, 512 threads: warp 0 issues TMA loads, warps 1-4 issue the
-// MMAs (one thread each, one per (slot, column half); warp 1 owns TMEM),
-// warps 0, 5, 14 and 15 (one per SM sub-partition) normalise a quarter of
-// every synthesis tile each, and two softmax warpgroups (warps 6-9 and
-// 10-13) take the first and the second 64 score columns of every step.
-// Both work on two TMEM slots in turn, so the tensor core computes one slot's
-// products and next scores while the softmax runs on the other. Each (slot,
-// half) is a pipeline of its own: its issuing thread adds the half's products
-// and then writes the half's next 64 score columns, and its warpgroup waits
-// for those alone. A thread spends ~50-80 cycles issuing one tcgen05.mma, so
-// four issuers keep the tensor pipe fed where one or two would not. Warp w
-// reads TMEM lanes 32*(w%4) .. +31.
+// One CTA per SM, 512 threads: warp 0 issues TMA loads, warps 1 and 2 issue
+// the MMAs of softmax warpgroups 0 and 1 (a whole warp runs each issuing
+// loop, one elected lane issues), warps 4, 5, 14 and 15 (one per SM
+// sub-partition) normalise a quarter of every synthesis tile each, and two
+// softmax warpgroups (warps 6-9 and 10-13) each carry one online-softmax
+// stream: in the split kernel warpgroup g takes token rows 64g .. 64g+63 of
+// every tile, in the decode kernel every other token tile. Warp w reads TMEM
+// lanes 32*(w%4) .. +31, so each sub-partition runs one warp of each stream.
 //
-// A slot holds 128 score columns and two accumulators, one per column half:
-// each half writes its P in bf16 over the first 32 of its own score columns,
-// and its products go to its own accumulator, so the two halves of a row are
-// two independent softmax streams (own reference, own accumulator) that meet
-// only at the end, in the same log-sum-exp merge as the splits. The next
-// scores are issued after the products that read P; the tensor core runs a
-// thread's MMAs in order.
+// A warpgroup owns 256 TMEM columns: three score buffers of 64 columns, its
+// accumulator (D values, the row sum, padding) and, in the split kernel, the
+// latent queries (bf16 pairs, the A operand of the score MMAs). Sub-step j of
+// a stream uses buffer j % 3: its issuing thread adds the products of step j
+// (which read P from buffer j % 3) and at once issues the scores of step j + 3
+// into the same buffer, so the softmax finds the scores of its next two steps
+// already computed and never waits for the issue-and-complete round trip of
+// the tensor core. The tensor core runs one thread's MMAs in order, so the
+// new scores overwrite P only after the products have read it.
 //
 // The softmax is one pass: p = 2^(s*c - r) against a reference r (an integer
-// in exp2 units) fixed before the tile; the first tile of a stream sets r
+// in exp2 units) fixed before the step; the first step of a stream sets r
 // from its own max. Whether some p reached 2 is read off the packed bf16
 // results (exponent field >= 128 <=> p >= 2, which also catches inf); only
 // then does the warp read its scores again, move r to 16 units above the
 // ceiling of their max and redo them, and the accumulator is rescaled
-// exactly by 2^(r_old - r_new) before the tile's products are added.
+// exactly by 2^(r_old - r_new) before the step's products are added, once
+// the products of the previous step are complete (the scores of step j + 2
+// were issued after them, so their barrier proves it; the issuing thread
+// issues two score sets past the end of its stream for this purpose).
 //
 // Every wait on an mbarrier is bounded: after about a second without progress
 // the thread records kErrTimeout in the device error word, raises the CTA's
@@ -60,6 +61,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -81,8 +83,8 @@ constexpr int kTraceRoles = 16, kTraceLen = 4096;
 __device__ unsigned long long g_trace[kTraceRoles][kTraceLen];
 __device__ int g_trace_pass = 0;
 // roles: kernel start/end; TMA issue per tile; N0 per tile (4 parts);
-// issuing threads (slot, half) per step; softmax warps of the two halves
-// per (step, slot); epilogue phases
+// issuing thread of each stream per step (3 stamps); first softmax warp of
+// each stream per step (2 stamps); epilogue phases
 enum : int { kTrStart = 0, kTrLoad = 1, kTrNorm = 2, kTrIssue = 6, kTrSoftmax = 10, kTrEpi = 12 };
 __device__ __forceinline__ void trace_stamp(bool on, int role, int i) {
   if (on && i >= 0 && i < kTraceLen) g_trace[role][i] = clock64();
@@ -93,38 +95,32 @@ __device__ __forceinline__ void trace_stamp(bool on, int role, int i) {
 #endif
 
 constexpr int kThreads = 512;
-constexpr int kWarpIssue = 1;        // first MMA-issuing warp: warp 1 + 2k + hf
-constexpr int kWarpNorm = 5;         // N0 of the synthesis tiles: warps 0, 5, 14 and 15
-constexpr int kWarpSoftmax = 6;      // first softmax warp (6-13)
+constexpr int kWarpIssue = 1;        // MMA-issuing warps: 1 + stream
+constexpr int kWarpNorm = 5;         // N0 of the synthesis tiles: warps 4, 5, 14 and 15
+constexpr int kWarpSoftmax = 6;      // first softmax warp (6-13): stream (w - 6) / 4
 constexpr int kTile = 128;           // tokens per staged tile; latents per row block
 constexpr int kMaxStages = 16;       // token-tile ring depth (upper bound)
+constexpr int kBufs = 3;             // score buffers per stream
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSlotCols = 256;  // slot s starts at column 256*s
-constexpr uint32_t kColO = 128;      // accumulator of column half 0; half 1's follows it
-constexpr uint32_t kColQ = 224;      // the slot's latent queries (bf16 pairs), A operand of the scores
+constexpr uint32_t kGroupCols = 256;  // stream g owns columns 256g .. 256g+255
+constexpr uint32_t kColO = 192;       // the stream's accumulator
+constexpr uint32_t kColQ = 240;       // split kernel: the latent queries (bf16 pairs)
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
 // under the test hook that makes one barrier never complete, waits give up
 // after ~1 ms, so that the forced timeout ends the call quickly
 constexpr long long kTestWaitLimit = 2000000LL;
-
-// How the two TMEM slots of a split-kernel CTA divide the work:
-//  kLanes   (M <= 64)  each slot holds the latents twice; lanes 0-63 and 64-127
-//                      score different token tiles (4 token streams per CTA);
-//  kStreams            one 128-row latent block, the slots take alternate tiles;
-//  kPair               two 128-row latent blocks, both slots see every tile.
-enum : int { kLanes = 0, kStreams = 1, kPair = 2 };
 
 struct Shared {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t norm[kMaxStages];
   uint64_t q_full;
-  uint64_t s_full[2][2];  // scores of half h of slot k ready (and the half's earlier products done)
-  uint64_t p_full[2][2];  // P of column half h of slot k written
-  uint64_t o_full[2][2];  // the last products of half h of slot k done
-  uint64_t q_tmem;        // the latent queries are in TMEM
-  uint64_t drain;         // every MMA of the CTA has completed
-  long long wait_limit;   // clock cycles a wait may take before it gives up
+  uint64_t s_full[2][kBufs];  // scores of stream g in buffer b ready (and the stream's earlier products done)
+  uint64_t p_full[2][kBufs];  // P of stream g in buffer b written
+  uint64_t o_full[2];         // split: every product of stream g done; decode: a tile's products done
+  uint64_t q_tmem[2];         // split: the latent queries are in stream g's columns
+  uint64_t drain;             // every MMA of the CTA has completed
+  long long wait_limit;       // clock cycles a wait may take before it gives up
   uint32_t tmem_base;
   int abort;
   int last;
@@ -195,6 +191,8 @@ struct Layout {
     return r * kRowBytes + ((c ^ x) << 4);
   }
 };
+static_assert(kColO + Layout<32>::kNo <= kColQ && kColQ + 16 <= kGroupCols, "a stream's TMEM columns overlap");
+static_assert(kBufs * 64 <= kColO, "score buffers overlap the accumulator");
 
 // Fills a 128-row tile, in the swizzled layout of the value tiles, with rows
 // [1, 0, ..., 0]: as the extra column block of an MN-major B operand it makes
@@ -245,20 +243,21 @@ __device__ __forceinline__ float load_acc(uint32_t tO, float (&o)[D]) {
 }
 
 // ------------------------------------------------------------- softmax step
-// Reads this lane's 64 scores of a column half and masks the columns at or
-// past `valid` (1..64).
-__device__ __forceinline__ void load_half(uint32_t tS, int valid, uint32_t (&s)[64]) {
-  tmem_ld64(tS, s);
-  tmem_wait_ld_regs(s);
-  if (valid < 64) {
-#pragma unroll
-    for (int i = 0; i < 64; ++i)
-      if (i >= valid) s[i] = __float_as_uint(-INFINITY);
-  }
-}
+// Exponent field >= 128 in either bf16 half: some p >= 2 (or inf / NaN).
+constexpr uint32_t kGrowBits = 0x40004000u;
+// When the reference moves it is set this many exp2 units above the tile max,
+// so that p <= 2^-16 and the next move waits for the max to grow by 17 units
+// (p that small loses nothing: fp32 and bf16 keep their relative precision
+// down to 2^-126).
+constexpr float kHeadroom = 16.0f;
 
-// p = 2^(s*c - r) of the 64 columns, packed in bf16 pairs into s[0..31];
-// returns the OR of the packed words.
+// P (32 packed words) goes over the second half of a step's 64 score
+// columns, so that the first half stays in TMEM for a step that is redone.
+constexpr uint32_t kColP = 32;
+
+// p = 2^(s*c - r) of the 64 scores, packed in bf16 pairs over s[0..31]
+// (word i is written after scores 2i and 2i + 1 are read, so the scores
+// 32..63 stay in s[32..63]); returns the OR of the packed words.
 __device__ __forceinline__ uint32_t exp_pack(uint32_t (&s)[64], float c, float r) {
   const float2 cc = make_float2(c, c);
   const float2 rr = make_float2(-r, -r);
@@ -273,15 +272,7 @@ __device__ __forceinline__ uint32_t exp_pack(uint32_t (&s)[64], float c, float r
   return o0 | o1;
 }
 
-// Exponent field >= 128 in either bf16 half: some p >= 2 (or inf / NaN).
-constexpr uint32_t kGrowBits = 0x40004000u;
-// When the reference moves it is set this many exp2 units above the tile max,
-// so that p <= 2^-16 and the next move waits for the max to grow by 17 units
-// (p that small loses nothing: fp32 and bf16 keep their relative precision
-// down to 2^-126).
-constexpr float kHeadroom = 16.0f;
-
-__device__ __forceinline__ float half_max(const uint32_t (&s)[64]) {
+__device__ __forceinline__ float max64(const uint32_t (&s)[64]) {
   float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
   for (int i = 0; i < 64; i += 4) {
@@ -291,42 +282,70 @@ __device__ __forceinline__ float half_max(const uint32_t (&s)[64]) {
   return fmaxf(m0, m1);
 }
 
-// One softmax step of this lane over its column half at tS: `valid` (<= 64)
-// columns, P (32 packed columns) written over the first 32. The first tile
-// of a stream (r = -inf, the same for the whole warp) takes its reference
-// from its own max; later tiles are done against r in one pass, and only if
-// some p reached 2 is the half read again and redone against a new r.
-// Warp-uniform `valid`.
-__device__ __forceinline__ void softmax_half(uint32_t tS, int valid, float c, float& r) {
-  uint32_t s[64];
-  load_half(tS, valid, s);
-  if (__any_sync(0xFFFFFFFFu, r == -INFINITY)) {
-    const float m = half_max(s);
-    if (r == -INFINITY) r = ceilf(m * c) + kHeadroom;
-    exp_pack(s, c, r);
-  } else {
-    const uint32_t bits = exp_pack(s, c, r);
-    if (__any_sync(0xFFFFFFFFu, (bits & kGrowBits) != 0u)) {
-      // the scores are still in TMEM
-      load_half(tS, valid, s);
-      const float m = half_max(s);
-      if ((bits & kGrowBits) != 0u) r = ceilf(m * c) + kHeadroom;
-      exp_pack(s, c, r);
-    }
-  }
-  tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(s));
+// Scores of the columns at or past `valid` set to -inf.
+__device__ __forceinline__ void mask64(uint32_t (&s)[64], int valid) {
+#pragma unroll
+  for (int i = 0; i < 64; ++i)
+    if (i >= valid) s[i] = __float_as_uint(-INFINITY);
 }
 
-// End of a softmax step: the products of the previous step are in (this
-// step's scores were issued after them), so the accumulator is brought to the
-// reference of the probabilities just written; then P goes to the tensor core.
+// One softmax step of this lane over the 64 score columns at tS, P stored
+// over columns 32-63. `kMasked`: columns at or past `valid` count as absent
+// (only a stream's last step); `first` (the same in every lane of the warp):
+// the stream's first step, whose reference comes from its own max. Later
+// steps are done against r in one pass; only if some p reached 2 do those
+// lanes move r to 16 units above the ceiling of their max and redo P, with
+// the first half of the scores read again from TMEM (the second half is
+// still in registers). Returns whether that happened (the same in every
+// lane); `r_old` then holds the reference before the move.
+template <bool kMasked>
+__device__ __forceinline__ bool softmax_step(uint32_t tS, int valid, bool first, float c, float& r, float& r_old) {
+  uint32_t s[64];
+  tmem_ld64(tS, s);
+  tmem_wait_ld_regs(s);
+  if (kMasked) mask64(s, valid);
+  if (first) r = ceilf(max64(s) * c) + kHeadroom;
+  const uint32_t bits = exp_pack(s, c, r);
+  tmem_st32(tS + kColP, *reinterpret_cast<uint32_t(*)[32]>(s));
+  if (!__any_sync(0xFFFFFFFFu, (bits & kGrowBits) != 0u)) return false;
+  tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(s));
+  tmem_wait_ld_regs(s);
+  if (kMasked) mask64(s, valid);
+  r_old = r;
+  if ((bits & kGrowBits) != 0u) r = ceilf(max64(s) * c) + kHeadroom;
+  tmem_wait_st();  // the first store has landed before it is overwritten
+  exp_pack(s, c, r);
+  tmem_st32(tS + kColP, *reinterpret_cast<uint32_t(*)[32]>(s));
+  return true;
+}
+
+// Writes P = 0 (a step with no token).
+__device__ __forceinline__ void zero_p(uint32_t tS) {
+  uint32_t z[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) z[i] = 0u;
+  tmem_st32(tS + kColP, z);
+}
+
+// End of a softmax step: if the step was redone (`moved`, the same in every
+// lane), the accumulator of each lane whose reference moved from r_old to r
+// is brought to the new one, once the stream's previous products are
+// complete (`proof`, the barrier of scores issued after them, phase
+// `proof_parity`); then P goes to the tensor core (one arrival per warp).
 template <int D>
-__device__ __forceinline__ void finish_half(uint64_t* p_full, uint32_t tO, float r, float& ro, bool acc) {
+__device__ __forceinline__ bool finish_step(Shared& sh, uint64_t* p_full, uint32_t tO, float r, float r_old,
+                                            bool acc, bool moved, uint64_t* proof, uint32_t proof_parity) {
+  bool ok = true;
+  if (moved) {
+    ok = warp_wait(sh, proof, proof_parity);
+    tc_fence_after();
+    if (ok) rescale_acc<D>(tO, acc && r_old != r ? pow2_neg(r_old - r) : 1.f);
+  }
   tmem_wait_st();
-  const bool need = acc && ro != r;
-  if (__any_sync(0xFFFFFFFFu, need)) rescale_acc<D>(tO, need ? pow2_neg(ro - r) : 1.f);
-  ro = r;
-  warp_arrive(p_full);
+  tc_fence_before();
+  __syncwarp();
+  mbar_arrive_if(p_full, (threadIdx.x & 31) == 0);
+  return ok;
 }
 
 // N0 (eq. 5) of rows 32*part + lane of staged synthesis tile t, in place, in
@@ -372,67 +391,69 @@ struct SplitParams {
   int N, M, H, qtiles, splits, split_len;
   float* part_z;            // [BH][qtiles][splits][128][D]
   float* part_l;            // [BH][qtiles][splits][128]
-  unsigned* counters;       // [BH][qgroups]
+  unsigned* counters;       // [BH][qtiles]
   int q_by_head;            // latent queries [H][M][D] (1) or [BH][M][D] (0)
   const __nv_bfloat16* qf;  // gated passes: [H][M][D]
   const float* gate;        // gated passes: [H]
   __nv_bfloat16* out;       // gated: Q; encode: Z ([BH][M][D])
   float* dbg_a;             // gated: Qd; encode: Z (as rounded)
   float* dbg_b;             // gated: Q (as rounded); encode: L
-  int fail_wait;            // test only: P barrier of slot 0, half 0 expects one arrival too many
+  int fail_wait;            // test only: P barrier of stream 0, buffer 0 expects one arrival too many
 };
 
-struct SlotPlan {
-  int mode;
-  int qt[2];     // latent block of each slot
-  int steps[2];  // steps each slot processes
-};
-
-__device__ __forceinline__ SlotPlan slot_plan(int M, int qtiles, int group, int T) {
-  SlotPlan s;
-  if (M <= 64) {
-    s.mode = kLanes;
-    s.qt[0] = s.qt[1] = 0;
-  } else if (2 * group + 1 < qtiles) {
-    s.mode = kPair;
-    s.qt[0] = 2 * group;
-    s.qt[1] = 2 * group + 1;
-  } else {
-    s.mode = kStreams;
-    s.qt[0] = s.qt[1] = 2 * group;
-  }
-  for (int k = 0; k < 2; ++k) {
-    if (s.mode == kLanes) s.steps[k] = T > 2 * k ? (T - 2 * k + 3) / 4 : 0;
-    else if (s.mode == kStreams) s.steps[k] = T > k ? (T - k + 1) / 2 : 0;
-    else s.steps[k] = T;
-  }
-  return s;
-}
-
-// Token tile of slot k at step j (in the lanes mode lanes 64-127 take tile + 1).
-__device__ __forceinline__ int slot_tile(const SlotPlan& s, int k, int j) {
-  if (s.mode == kLanes) return 4 * j + 2 * k;
-  if (s.mode == kStreams) return 2 * j + k;
-  return j;
-}
-
-// Epilogue scratch of the split kernel: (L, Z) of 512 softmax streams.
+// Epilogue scratch of the split kernel: (L, Z) of 256 softmax streams.
 template <int D>
 __host__ __device__ constexpr int split_scratch_bytes() {
-  return 512 * 4 + 512 * (D + 1) * 4;
+  return 256 * 4 + 256 * (D + 1) * 4;
 }
 
 // Token-tile ring depth of the split kernel: as deep as fits next to the
-// latent tiles and the ones tile (within ~200 KB). A stage holds a key tile,
+// latent tile and the ones tile (within ~200 KB). A stage holds a key tile,
 // and a value tile unless the keys serve as values.
 template <int D, int kKind>
 __host__ __device__ constexpr int split_stages() {
   constexpr int stage = (pass_separate_values(kKind) ? 2 : 1) * Layout<D>::kTileBytes;
-  constexpr int n = (200 * 1024 - 3 * Layout<D>::kTileBytes) / stage;
+  constexpr int n = (200 * 1024 - 2 * Layout<D>::kTileBytes) / stage;
   return n > kMaxStages ? kMaxStages : n;
 }
 
+// The finished row of a latent block (merged over all token splits): the
+// gated passes write Q = N0(Qf) + g * u (eq. 7) in bf16, the encode Z = u in
+// bf16 and its log-normaliser; the fp32 copies are for stage-level checks.
 template <int D, int kKind>
+__device__ __forceinline__ void write_final(const SplitParams& p, int bh, int h, int latent, float (&u)[D],
+                                            float lse) {
+  const size_t orow = (size_t)bh * p.M + latent;
+  if (pass_gated(kKind)) {
+    float f[D];
+    load_row<D>(p.qf + ((size_t)h * p.M + latent) * D, f);
+    float ss = 0.f;
+#pragma unroll
+    for (int d = 0; d < D; ++d) ss = fmaf(f[d], f[d], ss);
+    const float rr = rsqrtf(ss / (float)D + kEps);
+    const float g = p.gate[h];
+    float q[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) q[d] = fmaf(g, u[d], f[d] * rr);
+    store_row<D>(p.out + orow * D, q);
+    if (p.dbg_a) store_row<D>(p.dbg_a + orow * D, u);
+    if (p.dbg_b) {
+#pragma unroll
+      for (int d = 0; d < D; ++d) q[d] = round_as<__nv_bfloat16>(q[d]);
+      store_row<D>(p.dbg_b + orow * D, q);
+    }
+  } else {
+    store_row<D>(p.out + orow * D, u);
+    if (p.dbg_a) {
+#pragma unroll
+      for (int d = 0; d < D; ++d) u[d] = round_as<__nv_bfloat16>(u[d]);
+      store_row<D>(p.dbg_a + orow * D, u);
+    }
+    if (p.dbg_b) p.dbg_b[orow] = lse;
+  }
+}
+
+template <int D, int kKind, bool kLanes>
 __global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
@@ -442,41 +463,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStages = split_stages<D, kKind>();
   constexpr uint32_t kStageBytes = kSepValues ? 2 * L::kTileBytes : L::kTileBytes;
   constexpr uint32_t kValueOff = kSepValues ? L::kTileBytes : 0;  // value tile within a stage
+  // tiles per step: M <= 64 ("lanes" layout): TMEM lanes 64-127 repeat the
+  // latents of lanes 0-63 and score the next token tile
+  constexpr int kTps = kLanes ? 2 : 1;
   static_assert(kStages * (int)kStageBytes >= split_scratch_bytes<D>(), "epilogue scratch exceeds the stage ring");
+  static_assert(kStages > (kBufs + 1) * kTps, "the ring must hold the tiles of the scores issued ahead");
   extern __shared__ unsigned char smem_raw[];
   __shared__ Shared sh;
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-  unsigned char* sQ = smem;                                   // [2][128][D]
-  unsigned char* sStage = smem + 2 * L::kTileBytes;           // [kStages] x (K, V)
+  unsigned char* sQ = smem;                                   // [128][D]
+  unsigned char* sStage = smem + L::kTileBytes;               // [kStages] x (K, V)
   unsigned char* sOnes = sStage + kStages * kStageBytes;      // [128][D] rows [1, 0, ...]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int split = blockIdx.x, group = blockIdx.y, bh = blockIdx.z;
+  const int split = blockIdx.x, qt = blockIdx.y, bh = blockIdx.z;
   const int h = bh % p.H;
   const int n_begin = split * p.split_len;
   const int n_end = min(p.N, n_begin + p.split_len);
   const int T = n_begin < n_end ? (n_end - n_begin + kTile - 1) / kTile : 0;
-  const SlotPlan sp = slot_plan(p.M, p.qtiles, group, T);
-  const int jmax = max(sp.steps[0], sp.steps[1]);
+  const int U = (T + kTps - 1) / kTps;  // steps of each stream
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], sp.mode == kPair ? 4 : 2);  // one release per issuing thread that reads the tile
-      mbar_init(&sh.norm[s], 4);                          // one arrival per normaliser warp
+      mbar_init(&sh.empty[s], 2);  // one release per stream
+      mbar_init(&sh.norm[s], 4);   // one arrival per normaliser warp
     }
     mbar_init(&sh.q_full, 1);
-    for (int k = 0; k < 2; ++k)
-      for (int hf = 0; hf < 2; ++hf) {
-        mbar_init(&sh.s_full[k][hf], 1);
-        // one arrival per softmax warp of the half (one more under the test hook)
-        mbar_init(&sh.p_full[k][hf], 4 + (p.fail_wait && k == 0 && hf == 0 ? 1 : 0));
-        mbar_init(&sh.o_full[k][hf], 1);
+    for (int g = 0; g < 2; ++g) {
+      for (int b = 0; b < kBufs; ++b) {
+        mbar_init(&sh.s_full[g][b], 1);
+        // one arrival per softmax warp of the stream (one more under the test hook)
+        mbar_init(&sh.p_full[g][b], 4 + (p.fail_wait && g == 0 && b == 0 ? 1 : 0));
       }
-    mbar_init(&sh.drain, 4);
-    mbar_init(&sh.q_tmem, 4);
+      mbar_init(&sh.o_full[g], 1);
+      mbar_init(&sh.q_tmem[g], 4);
+    }
+    mbar_init(&sh.drain, 2);
     sh.wait_limit = p.fail_wait ? kTestWaitLimit : kWaitLimit;
     sh.abort = 0;
     sh.last = 0;
@@ -500,181 +525,182 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // (in the synthesis instance the warp also normalises rows 0-31 of each
-    // tile, kStages / 2 tiles behind the loads its lane 0 issues: the load of
-    // tile t waits for tile t - kStages to be released, which in the lanes
-    // mode needs tile t - kStages + 1 normalised, so the lag must stay below
-    // kStages - 1)
-    constexpr int kLag = kNormKeys ? kStages / 2 : 0;
-    static_assert(kLag <= kStages - 2, "normaliser lag would deadlock the ring");
-    int issued = 0;
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       if (kSepValues) prefetch_tmap(&tm_v);
       const int qz = p.q_by_head ? h : bh;
-      mbar_arrive_expect_tx(&sh.q_full, (sp.mode == kPair ? 2 : 1) * L::kTileBytes);
-      if (sp.mode == kLanes) {
+      mbar_arrive_expect_tx(&sh.q_full, L::kTileBytes);
+      if (kLanes) {
         // the 64 (or fewer) latents twice: lanes 64-127 repeat lanes 0-63
         tma_load_3d(sQ, &tm_q, &sh.q_full, 0, 0, qz);
         tma_load_3d(sQ + L::kTileBytes / 2, &tm_q, &sh.q_full, 0, 0, qz);
       } else {
-        tma_load_3d(sQ, &tm_q, &sh.q_full, 0, sp.qt[0] * kTile, qz);
-        if (sp.mode == kPair) tma_load_3d(sQ + L::kTileBytes, &tm_q, &sh.q_full, 0, sp.qt[1] * kTile, qz);
+        tma_load_3d(sQ, &tm_q, &sh.q_full, 0, qt * kTile, qz);
       }
-    }
-    bool ok = true;
-    for (int t = 0; t < T + kLag; ++t) {
-      if (lane == 0 && ok && t < T) {
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
         const int s = t % kStages;
-        if (t >= kStages && !wait_or_abort<true>(sh, &sh.empty[s], ((t / kStages) - 1) & 1)) {
-          ok = false;
-        } else {
-          unsigned char* dst = sStage + s * kStageBytes;
-          mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
-          tma_load_3d(dst, &tm_k, &sh.full[s], 0, n_begin + t * kTile, bh);
-          if (kSepValues) tma_load_3d(dst + kValueOff, &tm_v, &sh.full[s], 0, n_begin + t * kTile, bh);
-          issued = t + 1;
-          FLAREPP_TR(tr_on, kTrLoad, t);
-        }
+        if (t >= kStages && !wait_or_abort<true>(sh, &sh.empty[s], ((t / kStages) - 1) & 1)) break;
+        unsigned char* dst = sStage + s * kStageBytes;
+        mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
+        tma_load_3d(dst, &tm_k, &sh.full[s], 0, n_begin + t * kTile, bh);
+        if (kSepValues) tma_load_3d(dst + kValueOff, &tm_v, &sh.full[s], 0, n_begin + t * kTile, bh);
+        issued = t + 1;
+        FLAREPP_TR(tr_on, kTrLoad, t);
       }
-      if (kNormKeys) {
-        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-        const int tn = t - kLag;
-        if (ok && tn >= 0) {
-          ok = normalise_part<D, kStages>(sh, sStage, kStageBytes, tn, 0, lane);
-          FLAREPP_TR(tr_on && ok && lane == 0, kTrNorm, tn);
-        }
+      if (*(volatile int*)&sh.abort) {
+        // let the copies still in flight land before the CTA leaves
+        for (int t = max(0, issued - kStages); t < issued; ++t)
+          mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, sh.wait_limit);
+        mbar_wait(&sh.q_full, 0, sh.wait_limit);
       }
     }
-    if (lane == 0 && *(volatile int*)&sh.abort) {
-      // let the copies still in flight land before the CTA leaves
-      for (int t = max(0, issued - kStages); t < issued; ++t)
-        mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, sh.wait_limit);
-      mbar_wait(&sh.q_full, 0, sh.wait_limit);
-    }
-  } else if (warp < kWarpNorm) {
-    // ---------------------------------- MMA of column half hf of slot kk
-    {  // the whole warp runs the issuing loop; one elected lane issues
-      const int kk = (warp - kWarpIssue) >> 1, hf = (warp - kWarpIssue) & 1;
-      const uint32_t aOnes = smem_u32(sOnes);
-      const uint32_t idS = idesc_bf16(128, 64, false, false);
-      const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
-      const uint32_t rows_off = hf * 64 * L::kRowBytes;  // first token row of the half in a tile
-      constexpr uint32_t kLo = 0u, kAll = 0xFFFFFFFFu;
-      // The plan in scalars (a slot index only known at run time would put the
-      // plan in local memory, and every step would wait for an L1 load):
-      // slot kk's step j works on tile t0 + dt * j (in the lanes mode lanes
-      // 64-127 take the next tile as well).
-      const bool lanes = sp.mode == kLanes;
-      const int nsteps = kk ? sp.steps[1] : sp.steps[0];
-      const int t0 = lanes ? 2 * kk : (sp.mode == kStreams ? kk : 0);
-      const int dt = lanes ? 4 : (sp.mode == kStreams ? 2 : 1);
-      const uint32_t dS = tmem + kk * kSlotCols + 64 * hf;
-      const uint32_t tQ = tmem + kk * kSlotCols + kColQ;
-      const uint32_t dO = tmem + kk * kSlotCols + kColO + hf * L::kNo;
-      const uint32_t aP = tmem + kk * kSlotCols + 64 * hf;
-      auto ready = [&](int t) -> bool {
-        return warp_wait(sh, kNormKeys ? &sh.norm[t % kStages] : &sh.full[t % kStages], (t / kStages) & 1);
-      };
-      // Descriptors of stage 0, built once; stage s is s * kStageBytes further:
-      // the key descriptor's start address moves by that much, and so does the
-      // value descriptor's, whose distance to the ones tile (its leading byte
-      // offset field) shrinks by as much. Both fields stay in range, so one
-      // 64-bit add per stage moves them.
-      const uint64_t dK0 = L::kmajor(smem_u32(sStage) + rows_off, 0);
-      const uint64_t dV0 = L::values1(smem_u32(sStage) + kValueOff, aOnes, 4 * hf);
-      constexpr uint64_t kStep = kStageBytes >> 4;
-      constexpr uint64_t kVStep = kStep - (kStep << 16);  // modulo 2^64
-      auto key_desc = [&](int t) { return dK0 + static_cast<uint64_t>(t % kStages) * kStep; };
-      auto val_desc = [&](int t) { return dV0 + static_cast<uint64_t>(t % kStages) * kVStep; };
-      // scores of the half's 64 token columns of tile t (and t + 1 in the
-      // lanes mode); the latent queries (A) are read from TMEM, the keys (B)
-      // from the staged tile
-      // tile t (and t + 1 in the lanes mode) staged and normalised; waited
-      // for while the issuer has nothing else to do
-      auto tile_ready = [&](int t) -> bool {
-        if (!ready(t)) return false;
-        return !(lanes && t + 1 < T) || ready(t + 1);
-      };
-      auto issue_s = [&](int t) -> bool {
-        if (lanes) {
-          const bool has_b = t + 1 < T;
-          tc_fence_after();
-          const uint64_t ka = key_desc(t);
+  } else if (warp == kWarpIssue || warp == kWarpIssue + 1) {
+    // ------------------------------------------------ MMAs of stream g
+    // The whole warp runs the issuing loop; one elected lane issues. The loop
+    // is unrolled over the three score buffers (their TMEM columns and
+    // barriers become constants); ring stages and descriptors advance by
+    // adds; the wait for the tiles of the scores issued ahead comes before
+    // the wait for P, so that from P to the new scores nothing waits.
+    const int g = warp - kWarpIssue;
+    const uint32_t gbase = tmem + g * kGroupCols;
+    const uint32_t tQ = gbase + kColQ, dO = gbase + kColO;
+    const uint32_t aOnes = smem_u32(sOnes);
+    const uint32_t idS = idesc_bf16(128, 64, false, false);
+    const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
+    constexpr uint32_t kLo = 0u, kAll = 0xFFFFFFFFu;
+    uint64_t* const ready_bar = kNormKeys ? sh.norm : sh.full;  // staged (and normalised) tiles
+    // Descriptors of stage 0: the stream's 64 token rows of the key tile
+    // (K-major) and its value slices 4g .. 4g+3 with the ones tile (MN-major).
+    // Stage s is s * kStageBytes further: the key descriptor's start address
+    // moves by that much, and so does the value descriptor's, whose distance
+    // to the ones tile (its leading byte offset field) shrinks by as much.
+    // Both fields stay in range, so one multiply-add per stage moves them.
+    const uint64_t dK0 = L::kmajor(smem_u32(sStage) + g * 64 * L::kRowBytes, 0);
+    const uint64_t dV0 = L::values1(smem_u32(sStage) + kValueOff, aOnes, 4 * g);
+    const uint64_t dDummy = L::kmajor(aOnes, 0);
+    constexpr uint64_t kStep = kStageBytes >> 4;
+    constexpr uint64_t kVStep = kStep - (kStep << 16);  // modulo 2^64
+    // scores side: first tile of the next step to score, its stage and phase
+    // parity; products side: stage of the first tile of the next step
+    int s_tile = 0, s_stage = 0, p_stage = 0;
+    uint32_t s_par = 0u;
+    auto next_stage = [](int st) { return st + 1 == kStages ? 0 : st + 1; };
+    // the tiles of the next step to score are staged (and normalised)
+    auto scores_ready = [&]() -> bool {
+      if (!warp_wait(sh, &ready_bar[s_stage], s_par)) return false;
+      if (kLanes && s_tile + 1 < T) {
+        const int s2 = next_stage(s_stage);
+        return warp_wait(sh, &ready_bar[s2], s2 == 0 ? s_par ^ 1u : s_par);
+      }
+      return true;
+    };
+    // scores of the next step into buffer b: the latent queries (A) from
+    // TMEM, the keys (B) from the staged tile; in the lanes layout lanes
+    // 64-127 score the next tile. Past the end (`real` false) the ones tile
+    // is scored: nothing reads it, its barrier only proves that the products
+    // issued before it are complete.
+    auto issue_s = [&](bool real, int b) {
+      const uint32_t dS = gbase + 64 * b;
+      if (!real) {
 #pragma unroll
-          for (int q = 0; q < D / 16; ++q)
-            mma_ts_masked_elect(dS, tQ + q * 8, L::adv(ka, 32 * q), idS, q > 0, kLo, kLo, kAll, kAll);
-          if (has_b) {
-            const uint64_t kb = key_desc(t + 1);
+        for (int k = 0; k < D / 16; ++k) mma_ts_elect(dS, tQ + k * 8, L::adv(dDummy, 32 * k), idS, k > 0);
+      } else {
+        const uint64_t ka = dK0 + static_cast<uint64_t>(s_stage) * kStep;
+        if (kLanes) {
 #pragma unroll
-            for (int q = 0; q < D / 16; ++q)
-              mma_ts_masked_elect(dS, tQ + q * 8, L::adv(kb, 32 * q), idS, q > 0, kAll, kAll, kLo, kLo);
+          for (int k = 0; k < D / 16; ++k)
+            mma_ts_masked_elect(dS, tQ + k * 8, L::adv(ka, 32 * k), idS, k > 0, kLo, kLo, kAll, kAll);
+          if (s_tile + 1 < T) {
+            const uint64_t kb = dK0 + static_cast<uint64_t>(next_stage(s_stage)) * kStep;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              mma_ts_masked_elect(dS, tQ + k * 8, L::adv(kb, 32 * k), idS, k > 0, kAll, kAll, kLo, kLo);
           }
         } else {
-          tc_fence_after();
-          const uint64_t ka = key_desc(t);
 #pragma unroll
-          for (int q = 0; q < D / 16; ++q) mma_ts_elect(dS, tQ + q * 8, L::adv(ka, 32 * q), idS, q > 0);
+          for (int k = 0; k < D / 16; ++k) mma_ts_elect(dS, tQ + k * 8, L::adv(ka, 32 * k), idS, k > 0);
         }
-        mma_commit_elect(&sh.s_full[kk][hf]);
-        return true;
-      };
-      // O_hf (+)= P_hf [V | 1]_hf for tile t (and t + 1): slices 4hf .. 4hf+3
-      // of the tile, P of the half at column 64hf of the slot
-      auto issue_pv = [&](int t, uint32_t first) {
-        const uint64_t va = val_desc(t);
-        if (lanes) {
-          const bool has_b = t + 1 < T;
+        s_tile += kTps;
+        s_stage += kTps;
+        if (s_stage >= kStages) {
+          s_stage -= kStages;
+          s_par ^= 1u;
+        }
+      }
+      mma_commit_elect(&sh.s_full[g][b]);
+    };
+    // O (+)= P [V | 1] of step j, P in buffer b
+    auto issue_pv = [&](int j, int b) {
+      const uint32_t aP = gbase + 64 * b + kColP;  // P over the buffer's second half
+      const uint32_t first = j > 0 ? 1u : 0u;
+      const uint64_t va = dV0 + static_cast<uint64_t>(p_stage) * kVStep;
+      if (kLanes) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          mma_ts_masked_elect(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kLo, kLo, kAll,
+                              kAll);
+        if (kTps * j + 1 < T) {
+          const uint64_t vb = dV0 + static_cast<uint64_t>(next_stage(p_stage)) * kVStep;
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            mma_ts_masked_elect(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kLo, kLo, kAll,
-                          kAll);
-          if (has_b) {
-            const uint64_t vb = val_desc(t + 1);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              mma_ts_masked_elect(dO, aP + i * 8, L::adv(vb, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kAll, kAll, kLo,
-                            kLo);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) mma_ts_elect(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
+            mma_ts_masked_elect(dO, aP + i * 8, L::adv(vb, i * 2 * L::kAtom), idO, i > 0 ? 1u : first, kAll, kAll,
+                                kLo, kLo);
         }
-      };
-      // the stage(s) of tile t can be refilled once this thread's products of
-      // them are done (every issuing thread that read them releases)
-      auto release = [&](int t) {
-        mma_commit_elect(&sh.empty[t % kStages]);
-        if (lanes && t + 1 < T) mma_commit_elect(&sh.empty[(t + 1) % kStages]);
-      };
-      bool ok = nsteps > 0 && warp_wait(sh, &sh.q_tmem, 0) && tile_ready(t0);
-      tc_fence_after();
-      if (ok) ok = issue_s(t0);
-      // Per step: the products that read P, then at once the next step's
-      // scores (its tile was waited for before P was), then the release of
-      // the tile: the path from P to the next scores holds no wait and one
-      // commit.
-      for (int j = 0, t = t0; ok && j < nsteps; ++j, t += dt) {
-        const bool more = j + 1 < nsteps;
-        if (more && !tile_ready(t + dt)) break;
-        if (!warp_wait(sh, &sh.p_full[kk][hf], j & 1)) break;
-        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * j);
-        tc_fence_after();
-        issue_pv(t, j > 0 ? 1u : 0u);
-        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * j + 1);
-        if (more) ok = issue_s(t + dt);
-        release(t);
-        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * j + 2);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mma_ts_elect(dO, aP + i * 8, L::adv(va, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
       }
-      // every MMA of this CTA completes before TMEM is released
-      mma_commit_elect(&sh.drain);
-      mbar_wait(&sh.drain, 0, sh.wait_limit);
+      p_stage += kTps;
+      if (p_stage >= kStages) p_stage -= kStages;
+    };
+    bool ok = U > 0 && warp_wait(sh, &sh.q_tmem[g], 0);
+    tc_fence_after();
+    // the first three score sets (past the end: proof-only sets)
+#pragma unroll
+    for (int b = 0; b < kBufs; ++b) {
+      if (!ok) break;
+      const bool real = b < U;
+      if (real && !scores_ready()) {
+        ok = false;
+        break;
+      }
+      issue_s(real, b);
     }
-  } else if (warp == kWarpNorm || warp >= kWarpSoftmax + 8) {
+    // Step j with buffer b: the products that read P, then at once the
+    // scores of step j + 3 into the same buffer (U + 1 is the last one
+    // issued). The stage of step j is released by the softmax warps once
+    // these scores are done (they were issued after the products).
+    auto step = [&](int j, int b, uint32_t par) -> bool {
+      const bool more = j + kBufs <= U + 1, real = j + kBufs < U;
+      if (real && !scores_ready()) return false;
+      if (!warp_wait(sh, &sh.p_full[g][b], par)) return false;
+      FLAREPP_TR(tr_on && lane == 0, kTrIssue + g, 3 * j);
+      tc_fence_after();
+      issue_pv(j, b);
+      FLAREPP_TR(tr_on && lane == 0, kTrIssue + g, 3 * j + 1);
+      if (more) issue_s(real, b);
+      FLAREPP_TR(tr_on && lane == 0, kTrIssue + g, 3 * j + 2);
+      return true;
+    };
+    uint32_t par = 0u;
+    for (int j = 0; ok && j < U; j += kBufs, par ^= 1u) {
+      ok = step(j, 0, par);
+      if (ok && j + 1 < U) ok = step(j + 1, 1, par);
+      if (ok && j + 2 < U) ok = step(j + 2, 2, par);
+    }
+    // every product of the stream is in before its accumulator is read, and
+    // every MMA of this CTA completes before TMEM is released
+    mma_commit_elect(&sh.o_full[g]);
+    mma_commit_elect(&sh.drain);
+    mbar_wait(&sh.drain, 0, sh.wait_limit);
+  } else if (warp == kWarpNorm - 1 || warp == kWarpNorm || warp >= kWarpSoftmax + 8) {
     // ------------------------------------------- N0 of the synthesis keys
+    // (rows 32p .. 32p+31 of every tile by warp 4, 5, 14, 15: one per SM
+    // sub-partition)
     if (kNormKeys) {
-      const int part = warp == kWarpNorm ? 1 : warp - (kWarpSoftmax + 6);  // 1, 2, 3
+      const int part = warp < kWarpSoftmax ? warp - (kWarpNorm - 1) : warp - (kWarpSoftmax + 6);  // 0, 1, 2, 3
       for (int t = 0; t < T; ++t) {
         if (!normalise_part<D, kStages>(sh, sStage, kStageBytes, t, part, lane)) break;
         FLAREPP_TR(tr_on && lane == 0, kTrNorm + part, t);
@@ -683,214 +709,206 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kWarpSoftmax && warp < kWarpSoftmax + 8) {
     // ------------------------------------------------- softmax + epilogue
     const int tid = threadIdx.x - 32 * kWarpSoftmax;  // 0..255
-    const int hf = tid >> 7;                           // column half
+    const int g = tid >> 7;                            // stream
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const int lanes_half = sp.mode == kLanes ? (row >> 6) : 0;
+    const uint32_t gbase = tmem + lane_base + g * kGroupCols;
+    const uint32_t tO = gbase + kColO;
+    const int lanes_half = kLanes ? (row >> 6) : 0;  // the same in every lane of a warp
     const float c = rsqrtf((float)D) * kLog2e;
 #ifdef FLAREPP_TRACE
     const bool tr_sm = tr_on && lane == 0 && (warp == kWarpSoftmax || warp == kWarpSoftmax + 4);
 #endif
-    float r[2] = {-INFINITY, -INFINITY}, ro[2] = {-INFINITY, -INFINITY};  // references of P and of O
-    bool acc[2] = {false, false};
-    bool ok = true;
-    if (hf == 0) {
-      // latent query row `row` of each slot's block from the staged tile into
-      // the slot's Q columns (lane = latent row, bf16 pairs)
-      ok = wait_or_abort(sh, &sh.q_full, 0);
-      if (ok) {
+    // latent query row `row` of the staged block into the stream's Q columns
+    // (lane = latent row, bf16 pairs)
+    bool ok = wait_or_abort(sh, &sh.q_full, 0);
+    if (ok) {
+      uint32_t w[D / 2];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const unsigned char* src = sQ + (sp.mode == kPair ? k * L::kTileBytes : 0);
-          uint32_t w[D / 2];
-#pragma unroll
-          for (int cc = 0; cc < D / 8; ++cc) {
-            const uint4 v = *reinterpret_cast<const uint4*>(src + L::chunk_offset(row, cc));
-            w[4 * cc] = v.x; w[4 * cc + 1] = v.y; w[4 * cc + 2] = v.z; w[4 * cc + 3] = v.w;
-          }
-          const uint32_t tQ = tmem + lane_base + k * kSlotCols + kColQ;
-          if (D == 32) tmem_st16(tQ, *reinterpret_cast<uint32_t(*)[16]>(w));
-          else tmem_st8(tQ, *reinterpret_cast<uint32_t(*)[8]>(w));
-        }
-        tmem_wait_st();
+      for (int cc = 0; cc < D / 8; ++cc) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sQ + L::chunk_offset(row, cc));
+        w[4 * cc] = v.x; w[4 * cc + 1] = v.y; w[4 * cc + 2] = v.z; w[4 * cc + 3] = v.w;
       }
-      warp_arrive(&sh.q_tmem);
+      if (D == 32) tmem_st16(gbase + kColQ, *reinterpret_cast<uint32_t(*)[16]>(w));
+      else tmem_st8(gbase + kColQ, *reinterpret_cast<uint32_t(*)[8]>(w));
+      tmem_wait_st();
     }
-    for (int j = 0; ok && j < jmax; ++j) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        if (!ok || j >= sp.steps[k]) continue;
-        const uint32_t tS = tmem + lane_base + k * kSlotCols + 64 * hf;
-        const uint32_t tO = tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo;
-        if (!wait_or_abort(sh, &sh.s_full[k][hf], j & 1)) { ok = false; continue; }
-        FLAREPP_TR(tr_sm, kTrSoftmax + hf, 4 * j + 2 * k);
-        tc_fence_after();
-        const int t = slot_tile(sp, k, j) + lanes_half;
-        bool wrote = false;
-        if (t < T) {
-          const int valid = min(kTile, n_end - (n_begin + t * kTile)) - 64 * hf;
-          if (valid > 0) {
-            softmax_half(tS, min(valid, 64), c, r[k]);
-            wrote = true;
-          } else {
-            // no token in this half of the last tile: P = 0
-            uint32_t z[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) z[i] = 0u;
-            tmem_st32(tS, z);
-          }
-        }
-        finish_half<D>(&sh.p_full[k][hf], tO, r[k], ro[k], acc[k]);
-        FLAREPP_TR(tr_sm, kTrSoftmax + hf, 4 * j + 2 * k + 1);
-        if (wrote) acc[k] = true;
+    warp_arrive(&sh.q_tmem[g]);
+    float r = -INFINITY, r_old = -INFINITY;  // the stream's reference (exp2 units)
+    bool acc = false;                         // the accumulator holds products
+    // One thread per stream releases the stage(s) of step j - 3 once the
+    // scores of step j are done: the issuing thread issued them after the
+    // products of step j - 3, the last reads of those stages by this stream.
+    const bool rel_warp = (warp & 3) == (kWarpSoftmax & 3);  // one warp of each stream
+    int rel_stage = 0;  // stage of the first tile of step j - 3
+    // the stream's token columns in the last tile (every earlier step has 64)
+    const int last_valid = min(kTile, n_end - (n_begin + (T - 1) * kTile)) - 64 * g;
+    int b = 0;
+    uint32_t par = 0u;  // phase parity of step j's barriers: (j / 3) & 1
+    // Step j. kLast: the stream's last step, where the tile may be partial or
+    // (lanes layout) absent; every other step is a full 64-column step with
+    // no test of its columns.
+    auto step = [&](int j, auto last_tag) -> bool {
+      constexpr bool kLast = decltype(last_tag)::value;
+      const uint32_t tS = gbase + 64 * b;
+      if (!wait_or_abort(sh, &sh.s_full[g][b], par)) return false;
+      FLAREPP_TR(tr_sm, kTrSoftmax + g, 2 * j);
+      tc_fence_after();
+      if (rel_warp && j >= kBufs) {
+        mbar_arrive_if(&sh.empty[rel_stage], lane == 0);
+        if (kLanes) mbar_arrive_if(&sh.empty[rel_stage + 1 == kStages ? 0 : rel_stage + 1], lane == 0 && kTps * (j - kBufs) + 1 < T);
+        rel_stage += kTps;
+        if (rel_stage >= kStages) rel_stage -= kStages;
       }
-    }
-    // every product is complete before the stage buffers are reused as
-    // scratch below
-    if (ok) ok = wait_or_abort(sh, &sh.drain, 0);
+      bool moved = false, wrote = true;
+      if (kLast) {
+        const int t = kTps * j + lanes_half;
+        const int valid = t + 1 < T ? 64 : (t < T ? last_valid : 0);  // the same in every lane of a warp
+        if (valid > 0) {
+          moved = softmax_step<true>(tS, min(valid, 64), j == 0, c, r, r_old);
+        } else {
+          wrote = false;
+          if (t < T) zero_p(tS);  // no token in the stream's half of the last tile
+        }
+      } else {
+        moved = softmax_step<false>(tS, 64, j == 0, c, r, r_old);
+      }
+      const int bp = b == 0 ? 2 : (b == 1 ? 0 : 1);  // buffer of step j + 2 and its phase
+      const bool ok2 = finish_step<D>(sh, &sh.p_full[g][b], tO, r, r_old, acc, moved, &sh.s_full[g][bp],
+                                      b == 0 ? par : par ^ 1u);
+      FLAREPP_TR(tr_sm, kTrSoftmax + g, 2 * j + 1);
+      if (wrote) acc = true;
+      if (b == kBufs - 1) {
+        b = 0;
+        par ^= 1u;
+      } else {
+        ++b;
+      }
+      return ok2;
+    };
+    using Full = std::false_type;
+    using Last = std::true_type;
+    for (int j = 0; ok && j + 1 < U; ++j) ok = step(j, Full{});
+    if (ok && U > 0) ok = step(U - 1, Last{});
+    // every product of the stream is in before the accumulator is read
+    if (ok && U > 0) ok = wait_or_abort(sh, &sh.o_full[g], 0);
     tc_fence_after();
     FLAREPP_TR(tr_on && tid == 0, kTrEpi, 0);
 
-    // 1) each softmax stream's (L, Z) into shared memory: stream e =
-    //    256 hf + 128 k + row
+    // 1) each stream's (L, Z) into shared memory, stream e = 128 g + row
+    //    (after the whole CTA's products are done: the scratch is the ring)
+    float o[D];
+    const float l = load_acc<D>(tO, o);
+    if (ok) ok = wait_or_abort(sh, &sh.drain, 0);
+    softmax_groups_sync();
     constexpr int kZs = D + 1;  // padded row stride
-    float* scr_l = reinterpret_cast<float*>(sStage);  // [512]
-    float* scr_z = scr_l + 512;                       // [512][D + 1]
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      float o[D];
-      const float l = load_acc<D>(tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo, o);
-      const int e = 256 * hf + 128 * k + row;
-      const bool any = ok && acc[k] && l > 0.f;  // a stream with no token never wrote its accumulator
+    float* scr_l = reinterpret_cast<float*>(sStage);  // [256]
+    float* scr_z = scr_l + 256;                       // [256][D + 1]
+    {
+      const int e = 128 * g + row;
+      const bool any = ok && acc && l > 0.f;  // a stream with no token never wrote its accumulator
       const float inv = any ? 1.f / l : 0.f;
-      scr_l[e] = any ? (ro[k] + __log2f(l)) * kLn2 : -INFINITY;
+      scr_l[e] = any ? (r + __log2f(l)) * kLn2 : -INFINITY;  // the accumulator is at reference r
 #pragma unroll
       for (int d = 0; d < D; ++d) scr_z[e * kZs + d] = any ? o[d] * inv : 0.f;
     }
     softmax_groups_sync();
 
-    // 2) one partial result per (latent row, split): the CTA's streams of a
-    //    row merged first (Appendix B.3 schedule over the streams). Stream e
-    //    belongs to latent row (e & 127) of block qt of slot (e >> 7) & 1; in
-    //    the lanes mode row r and r + 64 hold the same latent.
-    {
-      const int nwriters = sp.mode == kLanes ? 64 : (sp.mode == kStreams ? 128 : 256);
-      const int nent = 512 / nwriters;
-      for (int e = tid; e < nwriters; e += 256) {
-        const int r_w = e & 127;
-        const int qt_w = sp.mode == kPair && (e >> 7) ? sp.qt[1] : sp.qt[0];
-        const int latent_w = qt_w * kTile + r_w;
-        if (latent_w >= p.M) continue;
-        float lmax = -INFINITY;
-        for (int i = 0; i < nent; ++i) lmax = fmaxf(lmax, scr_l[e + i * nwriters]);
-        float u[D], dsum = 0.f;
-#pragma unroll
-        for (int d = 0; d < D; ++d) u[d] = 0.f;
-        for (int i = 0; i < nent; ++i) {
-          const float li = scr_l[e + i * nwriters];
-          const float w = li == -INFINITY ? 0.f : __expf(li - lmax);
-          dsum += w;
-#pragma unroll
-          for (int d = 0; d < D; ++d) u[d] = fmaf(w, scr_z[(e + i * nwriters) * kZs + d], u[d]);
-        }
-        const float invd = dsum > 0.f ? 1.f / dsum : 0.f;
-#pragma unroll
-        for (int d = 0; d < D; ++d) u[d] *= invd;
-        const size_t prow = (((size_t)bh * p.qtiles + qt_w) * p.splits + split) * kTile + r_w;
-        store_row<D>(p.part_z + prow * D, u);
-        p.part_l[prow] = dsum > 0.f ? lmax + __logf(dsum) : -INFINITY;
-      }
-    }
-    __threadfence();
-    softmax_groups_sync();
-    const size_t grp = (size_t)bh * gridDim.y + group;
-    FLAREPP_TR(tr_on && tid == 0, kTrEpi, 1);
-    if (tid == 0) {
-      const unsigned prev = atomicAdd(p.counters + grp, 1u);
-      sh.last = prev == (unsigned)(p.splits - 1);
-    }
-    softmax_groups_sync();
-    FLAREPP_TR(tr_on && tid == 0, kTrEpi, 2);
-    if (sh.last) {
-      __threadfence();
-      if (tid == 0) p.counters[grp] = 0u;  // ready for the next call
-      // 3) the last CTA of the group merges the splits (Appendix B.3:
-      //    L_max, d_s = exp(L_s - L_max), U = sum d_s Z_s, Z = U / d), with
-      //    `tpr` threads per latent row sharing the splits
-      const int rows = sp.mode == kLanes ? 64 : (sp.mode == kStreams ? 128 : 256);
-      const int tpr = 256 / rows;
-      const int rg = tid / tpr, part = tid % tpr;
-      const int qt_f = sp.mode == kPair && (rg >> 7) ? sp.qt[1] : sp.qt[0];
-      const int r_f = rg & 127;
-      const int latent_f = qt_f * kTile + r_f;
-      const size_t base = ((size_t)bh * p.qtiles + qt_f) * p.splits * kTile + r_f;
+    // 2) the CTA's streams of a latent row merged (Appendix B.3 schedule):
+    //    stream e holds latent row e & 127 (e & 63 in the lanes layout).
+    //    With one split this is the final result; otherwise one partial per
+    //    (latent row, split) and the last CTA of the head merges them.
+    const int nwriters = kLanes ? 64 : 128;
+    const int nent = 256 / nwriters;
+    for (int e = tid; e < nwriters; e += 256) {
+      const int latent = (kLanes ? 0 : qt * kTile) + e;
+      if (latent >= p.M) continue;
       float lmax = -INFINITY;
-#pragma unroll 4
-      for (int sidx = part; sidx < p.splits; sidx += tpr)
-        lmax = fmaxf(lmax, __ldcg(p.part_l + base + (size_t)sidx * kTile));
+      for (int i = 0; i < nent; ++i) lmax = fmaxf(lmax, scr_l[e + i * nwriters]);
       float u[D], dsum = 0.f;
 #pragma unroll
       for (int d = 0; d < D; ++d) u[d] = 0.f;
-#pragma unroll 2
-      for (int sidx = part; sidx < p.splits; sidx += tpr) {
-        const size_t rr = base + (size_t)sidx * kTile;
-        const float ls = __ldcg(p.part_l + rr);
-        const float w = ls == -INFINITY ? 0.f : __expf(ls - lmax);
+      for (int i = 0; i < nent; ++i) {
+        const float li = scr_l[e + i * nwriters];
+        const float w = li == -INFINITY ? 0.f : __expf(li - lmax);
         dsum += w;
-        const float4* zr = reinterpret_cast<const float4*>(p.part_z + rr * D);
 #pragma unroll
-        for (int d = 0; d < D; d += 4) {
-          const float4 zz = __ldcg(zr + d / 4);
-          u[d] = fmaf(w, zz.x, u[d]);
-          u[d + 1] = fmaf(w, zz.y, u[d + 1]);
-          u[d + 2] = fmaf(w, zz.z, u[d + 2]);
-          u[d + 3] = fmaf(w, zz.w, u[d + 3]);
+        for (int d = 0; d < D; ++d) u[d] = fmaf(w, scr_z[(e + i * nwriters) * kZs + d], u[d]);
+      }
+      const float invd = dsum > 0.f ? 1.f / dsum : 0.f;
+#pragma unroll
+      for (int d = 0; d < D; ++d) u[d] *= invd;
+      const float lse = dsum > 0.f ? lmax + __logf(dsum) : -INFINITY;
+      if (p.splits == 1) {
+        write_final<D, kKind>(p, bh, h, latent, u, lse);
+      } else {
+        const size_t prow = (((size_t)bh * p.qtiles + qt) * p.splits + split) * kTile + e;
+        store_row<D>(p.part_z + prow * D, u);
+        p.part_l[prow] = lse;
+      }
+    }
+    if (p.splits > 1) {
+      __threadfence();
+      softmax_groups_sync();
+      const size_t grp = (size_t)bh * p.qtiles + qt;
+      FLAREPP_TR(tr_on && tid == 0, kTrEpi, 1);
+      if (tid == 0) {
+        const unsigned prev = atomicAdd(p.counters + grp, 1u);
+        sh.last = prev == (unsigned)(p.splits - 1);
+      }
+      softmax_groups_sync();
+      FLAREPP_TR(tr_on && tid == 0, kTrEpi, 2);
+      if (sh.last) {
+        __threadfence();
+        if (tid == 0) p.counters[grp] = 0u;  // ready for the next call
+        // 3) the last CTA of the block merges the splits (Appendix B.3:
+        //    L_max, d_s = exp(L_s - L_max), U = sum d_s Z_s, Z = U / d), with
+        //    `tpr` threads per latent row sharing the splits
+        const int rows = kLanes ? 64 : 128;
+        const int tpr = 256 / rows;
+        const int r_f = tid / tpr, part = tid % tpr;
+        const int latent_f = (kLanes ? 0 : qt * kTile) + r_f;
+        const size_t base = ((size_t)bh * p.qtiles + qt) * p.splits * kTile + r_f;
+        float lmax = -INFINITY;
+#pragma unroll 4
+        for (int sidx = part; sidx < p.splits; sidx += tpr)
+          lmax = fmaxf(lmax, __ldcg(p.part_l + base + (size_t)sidx * kTile));
+        float u[D], dsum = 0.f;
+#pragma unroll
+        for (int d = 0; d < D; ++d) u[d] = 0.f;
+#pragma unroll 2
+        for (int sidx = part; sidx < p.splits; sidx += tpr) {
+          const size_t rr = base + (size_t)sidx * kTile;
+          const float ls = __ldcg(p.part_l + rr);
+          const float w = ls == -INFINITY ? 0.f : __expf(ls - lmax);
+          dsum += w;
+          const float4* zr = reinterpret_cast<const float4*>(p.part_z + rr * D);
+#pragma unroll
+          for (int d = 0; d < D; d += 4) {
+            const float4 zz = __ldcg(zr + d / 4);
+            u[d] = fmaf(w, zz.x, u[d]);
+            u[d + 1] = fmaf(w, zz.y, u[d + 1]);
+            u[d + 2] = fmaf(w, zz.z, u[d + 2]);
+            u[d + 3] = fmaf(w, zz.w, u[d + 3]);
+          }
         }
-      }
-      // combine the tpr threads of a row (consecutive lanes of one warp)
-      float gmax = lmax;
-      for (int off = 1; off < tpr; off <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, off));
-      const float sc = lmax == -INFINITY ? 0.f : __expf(lmax - gmax);
-      dsum *= sc;
+        // combine the tpr threads of a row (consecutive lanes of one warp)
+        float gmax = lmax;
+        for (int off = 1; off < tpr; off <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, off));
+        const float sc = lmax == -INFINITY ? 0.f : __expf(lmax - gmax);
+        dsum *= sc;
 #pragma unroll
-      for (int d = 0; d < D; ++d) u[d] *= sc;
-      for (int off = 1; off < tpr; off <<= 1) {
-        dsum += __shfl_xor_sync(0xFFFFFFFFu, dsum, off);
+        for (int d = 0; d < D; ++d) u[d] *= sc;
+        for (int off = 1; off < tpr; off <<= 1) {
+          dsum += __shfl_xor_sync(0xFFFFFFFFu, dsum, off);
 #pragma unroll
-        for (int d = 0; d < D; ++d) u[d] += __shfl_xor_sync(0xFFFFFFFFu, u[d], off);
-      }
-      if (part == 0 && latent_f < p.M) {
-        const float invd = 1.f / dsum;
+          for (int d = 0; d < D; ++d) u[d] += __shfl_xor_sync(0xFFFFFFFFu, u[d], off);
+        }
+        if (part == 0 && latent_f < p.M) {
+          const float invd = dsum > 0.f ? 1.f / dsum : 0.f;
 #pragma unroll
-        for (int d = 0; d < D; ++d) u[d] *= invd;
-        const size_t orow = (size_t)bh * p.M + latent_f;
-        if (pass_gated(kKind)) {
-          // gate (eq. 7): Q = N0(Qf) + g * Qd in fp32, cast to bf16
-          float f[D];
-          load_row<D>(p.qf + ((size_t)h * p.M + latent_f) * D, f);
-          float ss = 0.f;
-#pragma unroll
-          for (int d = 0; d < D; ++d) ss = fmaf(f[d], f[d], ss);
-          const float rr = rsqrtf(ss / (float)D + kEps);
-          const float g = p.gate[h];
-          float q[D];
-#pragma unroll
-          for (int d = 0; d < D; ++d) q[d] = fmaf(g, u[d], f[d] * rr);
-          store_row<D>(p.out + orow * D, q);
-          if (p.dbg_a) store_row<D>(p.dbg_a + orow * D, u);
-          if (p.dbg_b) {
-#pragma unroll
-            for (int d = 0; d < D; ++d) q[d] = round_as<__nv_bfloat16>(q[d]);
-            store_row<D>(p.dbg_b + orow * D, q);
-          }
-        } else {
-          store_row<D>(p.out + orow * D, u);
-          if (p.dbg_a) {
-#pragma unroll
-            for (int d = 0; d < D; ++d) u[d] = round_as<__nv_bfloat16>(u[d]);
-            store_row<D>(p.dbg_a + orow * D, u);
-          }
-          if (p.dbg_b) p.dbg_b[orow] = gmax + __logf(dsum);
+          for (int d = 0; d < D; ++d) u[d] *= invd;
+          write_final<D, kKind>(p, bh, h, latent_f, u, dsum > 0.f ? gmax + __logf(dsum) : -INFINITY);
         }
       }
     }
@@ -910,7 +928,7 @@ struct DecodeParams {
   int heads;           // Q/Z slots in shared memory: the most heads one CTA's tiles span
   int q_by_head;       // routing queries [H][M][D] (1) or [BH][M][D] (0)
   __nv_bfloat16* out;  // [BH][N][D]
-  int fail_wait;       // test only: P barrier of slot 0, half 0 expects one arrival too many
+  int fail_wait;       // test only: P barrier of stream 0, buffer 0 expects one arrival too many
 };
 
 // Token-tile ring depth of the decode kernel: a compile-time constant, so
@@ -976,35 +994,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 1; i < kDecodeHeads; ++i) hs += t >= bnd[i] ? 1 : 0;
     return hs;
   };
-  // Schedule: each column half of a slot owns whole token tiles and runs over
-  // all M routes of its tile in `nsub` steps of 64 routes, carrying its online
+  // Schedule: stream g takes local tiles g, g + 2, g + 4, ... and runs over
+  // all M routes of a tile in `nsub` steps of 64 routes, carrying its online
   // softmax over M from one step to the next, so its accumulator ends as a
-  // whole output row and the two halves never exchange data. Step u of slot k
-  // works on tile pair g = 2 (u / nsub) + k: half hf takes local tile
-  // 2g + hf, routes 64 (u % nsub) .. +63.
+  // whole output row. Step j of the stream: its (j / nsub)-th tile, routes
+  // 64 (j % nsub) .. +63; counters advance without a division.
   const int nsub = (p.M + 63) / 64;
-  int steps[2];
-  {
-    const int G = (T + 1) / 2;
-    for (int k = 0; k < 2; ++k) steps[k] = (G > k ? (G - k + 1) / 2 : 0) * nsub;
-  }
-  const int umax = max(steps[0], steps[1]);
-  // local token tile of half hf of slot k's step u (may be past T when T is odd)
-  auto tile_of = [&](int k, int u, int hf) { return 2 * (2 * (u / nsub) + k) + hf; };
+  // steps of stream g (a run-time index into an array would put it in local
+  // memory)
+  auto stream_steps = [&](int g) { return (T > g ? (T - g + 1) / 2 : 0) * nsub; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], 1);  // a tile is read by one issuing thread
+      mbar_init(&sh.empty[s], 1);  // a tile is read by one stream
     }
     mbar_init(&sh.q_full, 1);
-    for (int k = 0; k < 2; ++k)
-      for (int hf = 0; hf < 2; ++hf) {
-        mbar_init(&sh.s_full[k][hf], 1);
-        mbar_init(&sh.p_full[k][hf], 4 + (p.fail_wait && k == 0 && hf == 0 ? 1 : 0));
-        mbar_init(&sh.o_full[k][hf], 1);
+    for (int g = 0; g < 2; ++g) {
+      for (int b = 0; b < kBufs; ++b) {
+        mbar_init(&sh.s_full[g][b], 1);
+        mbar_init(&sh.p_full[g][b], 4 + (p.fail_wait && g == 0 && b == 0 ? 1 : 0));
       }
-    mbar_init(&sh.drain, 4);
+      mbar_init(&sh.o_full[g], 1);
+    }
+    mbar_init(&sh.drain, 2);
     sh.wait_limit = p.fail_wait ? kTestWaitLimit : kWaitLimit;
     sh.abort = 0;
     fence_mbar_init();
@@ -1054,105 +1067,144 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&sh.q_full, 0, sh.wait_limit);
       }
     }
-  } else if (warp < kWarpNorm) {
-    {  // the whole warp runs the issuing loop; one elected lane issues
-      const int kk = (warp - kWarpIssue) >> 1, hf = (warp - kWarpIssue) & 1;
-      const uint32_t aZ = smem_u32(sZ), aOnes = smem_u32(sOnes);
-      const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
-      // descriptors built once; an MMA moves them with one add (a thread
-      // spends its issue slots on every instruction between MMAs). Routes
-      // 64b .. 64b+63 start 64b rows into the chunked Q (and Z) tiles.
-      const uint64_t dK0 = L::kmajor(smem_u32(sK), 0);
-      const uint64_t dQ0 = L::kmajor(smem_u32(sQ), 0);
-      const uint32_t idS64 = idesc_bf16(128, 64, false, false);
-      const uint32_t dS = tmem + kk * kSlotCols + 64 * hf;
-      const uint32_t dO = tmem + kk * kSlotCols + kColO + hf * L::kNo;
-      // scores of local tile t against routes 64b .. 64b+63 of its head, whose
-      // Q and Z sit `hoff` bytes into their arrays
-      // the K tile of local tile t staged (waited for at its first route
-      // block, while the issuer has nothing else to do)
-      auto tile_wait = [&](int t, int b) -> bool {
-        if (t >= T || b != 0) return true;
-        return warp_wait(sh, &sh.full[t % stages], (t / stages) & 1);
-      };
-      auto issue_s = [&](int t, int b, uint32_t hoff) -> bool {
-        if (t < T) {
-          const int s = t % stages;
-          tc_fence_after();
-          const int width = min(64, p.M - 64 * b);
-          const uint64_t a = L::adv(dK0, s * L::kTileBytes), bq = L::adv(dQ0, hoff + b * 64 * L::kRowBytes);
-          const uint32_t id = width >= 64 ? idS64 : idesc_bf16(128, width, false, false);
-#pragma unroll
-          for (int q = 0; q < D / 16; ++q) mma_ss_elect(dS, L::adv(a, 32 * q), L::adv(bq, 32 * q), id, q > 0);
-        }
-        mma_commit_elect(&sh.s_full[kk][hf]);
-        // the tile's last read: its stage may be refilled
-        if (t < T && b == nsub - 1) mma_commit_elect(&sh.empty[t % stages]);
-        return true;
-      };
-      // O_hf (+)= P_hf [Z | 1] over the route slices of block b
-      auto issue_pv = [&](int t, int b, uint32_t hoff) {
-        if (t >= T) return;
-        const int nsl = min(64, p.M - 64 * b) / 16;
-        const uint64_t v = L::values1(aZ + hoff + (b >> 1) * L::kTileBytes, aOnes, 4 * (b & 1));
-        const uint32_t aP = tmem + kk * kSlotCols + 64 * hf;
-        const uint32_t first = b > 0 ? 1u : 0u;
-        if (nsl == 4) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) mma_ts_elect(dO, aP + i * 8, L::adv(v, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
-        } else {
-          for (int i = 0; i < nsl; ++i) mma_ts_elect(dO, aP + i * 8, L::adv(v, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
-        }
-      };
-      // the step's tile and route block, advanced without a division
-      int t = tile_of(kk, 0, hf), b = 0;
-      uint32_t hoff = head_slot(t) * head_bytes;
-      const int nsteps = kk ? steps[1] : steps[0];  // no run-time array index: steps stays in registers
-      bool ok = nsteps > 0 && warp_wait(sh, &sh.q_full, 0) && tile_wait(t, b);
-      if (ok) ok = issue_s(t, b, hoff);
-      // Per step: the products that read P, then at once the next step's
-      // scores (whose tile was waited for before P was).
-      for (int u = 0; ok && u < nsteps; ++u) {
-        int tn = t, bn = b + 1;
-        uint32_t hn = hoff;
-        if (bn == nsub) {
-          bn = 0;
-          tn = t + 4;
-          hn = head_slot(tn) * head_bytes;
-        }
-        const bool more = u + 1 < nsteps;
-        if (more && !tile_wait(tn, bn)) break;
-        if (!warp_wait(sh, &sh.p_full[kk][hf], u & 1)) break;
-        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * u);
+  } else if (warp == kWarpIssue || warp == kWarpIssue + 1) {
+    // ------------------------------------------------ MMAs of stream g
+    // Kept short as in the split kernel: unrolled over the three score
+    // buffers, every ring stage, route block and descriptor moved by adds.
+    const int g = warp - kWarpIssue;
+    const uint32_t gbase = tmem + g * kGroupCols;
+    const uint32_t dO = gbase + kColO;
+    const uint32_t aOnes = smem_u32(sOnes);
+    const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
+    const uint32_t idS64 = idesc_bf16(128, 64, false, false);
+    // the last route block holds M - 64 (nsub - 1) routes (a multiple of 16)
+    const int wlast = p.M - 64 * (nsub - 1);
+    const uint32_t idSlast = idesc_bf16(128, wlast, false, false);
+    const int nsl_last = wlast / 16;
+    // Descriptors: the K tile of ring stage s (K-major) is s tiles past
+    // stage 0; routes 64b .. 64b+63 of the head at byte offset `hoff` are
+    // hoff + 64b rows past the start of Q (K-major) and of Z (MN-major, with
+    // the ones tile as its second column block, whose distance shrinks as
+    // far as the start moves).
+    const uint64_t dK0 = L::kmajor(smem_u32(sK), 0);
+    const uint64_t dQ0 = L::kmajor(smem_u32(sQ), 0);
+    const uint64_t dZ0 = L::values1(smem_u32(sZ), aOnes, 0);
+    const uint64_t dDummy = L::kmajor(aOnes, 0);
+    constexpr uint64_t kKStep = L::kTileBytes >> 4;
+    constexpr uint64_t kBlk = (64 * L::kRowBytes) >> 4;
+    constexpr uint64_t kZBlk = kBlk - (kBlk << 16);  // modulo 2^64
+    auto q_head = [&](uint32_t hoff) { return dQ0 + (hoff >> 4); };
+    auto z_head = [&](uint32_t hoff) { return dZ0 + (hoff >> 4) - (static_cast<uint64_t>(hoff >> 4) << 16); };
+    const int U = stream_steps(g);
+    // scores side: tile ts (local), block bs, its stage, phase parity and
+    // descriptors; products side: tile tp, block bp, its stage and Z
+    // descriptor
+    int ts = g, bs = 0, stage_s = g;
+    uint32_t par_s = 0u;
+    uint64_t ks = dK0 + static_cast<uint64_t>(g) * kKStep, qs = q_head(head_slot(g) * head_bytes);
+    int tp = g, bp = 0, stage_p = g;
+    uint64_t zp = z_head(head_slot(g) * head_bytes);
+    // scores of the next step into buffer b (past the end: the ones tile
+    // against itself, a proof-only set)
+    auto issue_s = [&](bool real, int b) -> bool {
+      const uint32_t dS = gbase + 64 * b;
+      if (real) {
+        if (bs == 0 && !warp_wait(sh, &sh.full[stage_s], par_s)) return false;
         tc_fence_after();
-        issue_pv(t, b, hoff);
-        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * u + 1);
-        if (more) ok = issue_s(tn, bn, hn);
-        else mma_commit_elect(&sh.o_full[kk][hf]);
-        FLAREPP_TR(tr_on && lane == 0, kTrIssue + 2 * kk + hf, 3 * u + 2);
-        t = tn;
-        b = bn;
-        hoff = hn;
+        const uint32_t id = bs == nsub - 1 ? idSlast : idS64;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) mma_ss_elect(dS, L::adv(ks, 32 * k), L::adv(qs, 32 * k), id, k > 0);
+        if (++bs == nsub) {
+          bs = 0;
+          ts += 2;
+          stage_s += 2;
+          if (stage_s >= stages) {
+            stage_s -= stages;
+            par_s ^= 1u;
+          }
+          ks = dK0 + static_cast<uint64_t>(stage_s) * kKStep;
+          qs = q_head(head_slot(ts) * head_bytes);
+        } else {
+          qs += kBlk;
+        }
+      } else {
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) mma_ss_elect(dS, L::adv(dDummy, 32 * k), L::adv(dDummy, 32 * k), idS64, k > 0);
       }
-      mma_commit_elect(&sh.drain);
-      mbar_wait(&sh.drain, 0, sh.wait_limit);
+      mma_commit_elect(&sh.s_full[g][b]);
+      return true;
+    };
+    // O (+)= P [Z | 1] over the route slices of the current block, P in
+    // buffer b; after a tile's last block its stage is released and its
+    // accumulator may be read out
+    auto issue_pv = [&](int b) {
+      const uint32_t aP = gbase + 64 * b + kColP;  // P over the buffer's second half
+      const uint32_t first = bp > 0 ? 1u : 0u;
+      if (bp < nsub - 1 || nsl_last == 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mma_ts_elect(dO, aP + i * 8, L::adv(zp, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
+      } else {
+        for (int i = 0; i < nsl_last; ++i)
+          mma_ts_elect(dO, aP + i * 8, L::adv(zp, i * 2 * L::kAtom), idO, i > 0 ? 1u : first);
+      }
+      if (++bp == nsub) {
+        mma_commit_elect(&sh.empty[stage_p]);
+        mma_commit_elect(&sh.o_full[g]);
+        bp = 0;
+        tp += 2;
+        stage_p += 2;
+        if (stage_p >= stages) stage_p -= stages;
+        zp = z_head(head_slot(tp) * head_bytes);
+      } else {
+        zp += kZBlk;
+      }
+    };
+    bool ok = U > 0 && warp_wait(sh, &sh.q_full, 0);
+    // the first three score sets
+#pragma unroll
+    for (int b = 0; b < kBufs; ++b) {
+      if (!ok) break;
+      ok = issue_s(b < U, b);
     }
+    auto step = [&](int j, int b, uint32_t par) -> bool {
+      if (!warp_wait(sh, &sh.p_full[g][b], par)) return false;
+      FLAREPP_TR(tr_on && lane == 0, kTrIssue + g, 3 * j);
+      tc_fence_after();
+      issue_pv(b);
+      FLAREPP_TR(tr_on && lane == 0, kTrIssue + g, 3 * j + 1);
+      if (j + kBufs <= U + 1 && !issue_s(j + kBufs < U, b)) return false;
+      FLAREPP_TR(tr_on && lane == 0, kTrIssue + g, 3 * j + 2);
+      return true;
+    };
+    uint32_t par = 0u;
+    for (int j = 0; ok && j < U; j += kBufs, par ^= 1u) {
+      ok = step(j, 0, par);
+      if (ok && j + 1 < U) ok = step(j + 1, 1, par);
+      if (ok && j + 2 < U) ok = step(j + 2, 2, par);
+    }
+    mma_commit_elect(&sh.drain);
+    mbar_wait(&sh.drain, 0, sh.wait_limit);
   } else if (warp >= kWarpSoftmax && warp < kWarpSoftmax + 8) {
     const int tid = threadIdx.x - 32 * kWarpSoftmax;  // 0..255
-    const int hf = tid >> 7;
+    const int g = tid >> 7;
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t gbase = tmem + lane_base + g * kGroupCols;
+    const uint32_t tO = gbase + kColO;
     const float c = rsqrtf((float)D) * kLog2e;
+    const int U = stream_steps(g);
 #ifdef FLAREPP_TRACE
     const bool tr_sm = tr_on && lane == 0 && (warp == kWarpSoftmax || warp == kWarpSoftmax + 4);
 #endif
-    float r[2] = {-INFINITY, -INFINITY}, ro[2] = {-INFINITY, -INFINITY};
-    bool acc[2] = {false, false};
-    // out = O / rowsum of this half's accumulator, for its own token tile t
-    auto emit = [&](int k, int t, bool live) {
-      if (!live || t >= T) return;
+    // out = O / rowsum of the accumulator, for local tile t (the i-th of the
+    // stream), once the tile's products are done
+    auto emit = [&](int i, int t) -> bool {
+      const bool done = wait_or_abort(sh, &sh.o_full[g], i & 1);
+      tc_fence_after();
+      if (!done) return false;
       float z[D];
-      const float l = load_acc<D>(tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo, z);
+      const float l = load_acc<D>(tO, z);
       const int hs = head_slot(t);
       const int tok = (first + t - hs * n_tiles) * kTile + row;
       if (tok < p.N) {
@@ -1161,48 +1213,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int d = 0; d < D; ++d) z[d] *= inv;
         store_row<D>(p.out + ((size_t)(h0 + hs) * p.N + tok) * D, z);
       }
+      return true;
     };
     bool ok = true;
-    // the step's route block (the same for both slots) and each slot's tile
-    int b = 0;
-    int tk[2] = {tile_of(0, 0, hf), tile_of(1, 0, hf)};
-    for (int u = 0; u < umax; ++u) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        if (u >= steps[k]) continue;
-        const uint32_t tS = tmem + lane_base + k * kSlotCols + 64 * hf;
-        const uint32_t tO = tmem + lane_base + k * kSlotCols + kColO + hf * Layout<D>::kNo;
-        ok = ok && wait_or_abort(sh, &sh.s_full[k][hf], u & 1);
-        FLAREPP_TR(tr_sm, kTrSoftmax + hf, 4 * u + 2 * k);
-        tc_fence_after();
-        if (b == 0) {
-          // the previous tile's products are in: its output goes out before
-          // this step's products overwrite the accumulator
-          if (u > 0) emit(k, tk[k] - 4, ok);
-          r[k] = -INFINITY;
-          acc[k] = false;
-        }
-        if (!ok) continue;
-        const int valid = tk[k] < T ? min(64, p.M - 64 * b) : 0;
-        if (valid > 0) softmax_half(tS, valid, c, r[k]);
-        finish_half<D>(&sh.p_full[k][hf], tO, r[k], ro[k], acc[k]);
-        FLAREPP_TR(tr_sm, kTrSoftmax + hf, 4 * u + 2 * k + 1);
-        if (valid > 0) acc[k] = true;
-      }
-      if (++b == nsub) {
-        b = 0;
-        tk[0] += 4;
-        tk[1] += 4;
-      }
-    }
-    // the last tile of each slot
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      if (steps[k] == 0) continue;
-      const bool done = ok && wait_or_abort(sh, &sh.o_full[k][hf], 0);
+    float r = -INFINITY, r_old = -INFINITY;  // the reference of the current tile's stream over M
+    bool acc = false;                         // the accumulator holds this tile's products
+    const int wlast = p.M - 64 * (nsub - 1);  // routes of a tile's last block (16..64)
+    const int ntiles = T > g ? (T - g + 1) / 2 : 0;
+    int bf = 0, j = 0, i = 0;
+    uint32_t par = 0u;  // phase parity of step j's barriers: (j / 3) & 1
+    // Step j: route block b of the stream's i-th tile. kRagged: the last
+    // block of a tile when M is not a multiple of 64 (its columns at or past
+    // `wlast` count as absent); every other block has no test of its columns.
+    auto step = [&](int b, auto ragged_tag) -> bool {
+      constexpr bool kRagged = decltype(ragged_tag)::value;
+      const uint32_t tS = gbase + 64 * bf;
+      if (!wait_or_abort(sh, &sh.s_full[g][bf], par)) return false;
+      FLAREPP_TR(tr_sm, kTrSoftmax + g, 2 * j);
       tc_fence_after();
-      emit(k, tile_of(k, steps[k] - 1, hf), done);
+      // a new tile (b == 0) starts a new stream over M: its reference comes
+      // from its own first route block and its accumulator starts empty
+      if (b == 0) acc = false;
+      const bool moved = softmax_step<kRagged>(tS, kRagged ? wlast : 64, b == 0, c, r, r_old);
+      // the previous tile's output goes out before this step's products
+      // overwrite the accumulator
+      if (b == 0 && i > 0 && !emit(i - 1, g + 2 * (i - 1))) return false;
+      const int bp = bf == 0 ? 2 : (bf == 1 ? 0 : 1);  // buffer of step j + 2 and its phase
+      const bool ok2 = finish_step<D>(sh, &sh.p_full[g][bf], tO, r, r_old, acc, moved, &sh.s_full[g][bp],
+                                      bf == 0 ? par : par ^ 1u);
+      FLAREPP_TR(tr_sm, kTrSoftmax + g, 2 * j + 1);
+      acc = true;
+      if (bf == kBufs - 1) {
+        bf = 0;
+        par ^= 1u;
+      } else {
+        ++bf;
+      }
+      ++j;
+      return ok2;
+    };
+    using Full = std::false_type;
+    using Ragged = std::true_type;
+    for (i = 0; ok && i < ntiles; ++i) {
+      for (int b = 0; ok && b + 1 < nsub; ++b) ok = step(b, Full{});
+      if (ok) ok = wlast < 64 ? step(nsub - 1, Ragged{}) : step(nsub - 1, Full{});
     }
+    // the stream's last tile
+    if (ok && ntiles > 0) emit(ntiles - 1, g + 2 * (ntiles - 1));
   }
   tc_fence_before();
   __syncthreads();
@@ -1215,7 +1272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int kKind>
 size_t split_smem() {
   const size_t stage = (pass_separate_values(kKind) ? 2 : 1) * (size_t)Layout<D>::kTileBytes;
-  return 1024 + 3 * (size_t)Layout<D>::kTileBytes + split_stages<D, kKind>() * stage;
+  return 1024 + 2 * (size_t)Layout<D>::kTileBytes + split_stages<D, kKind>() * stage;
 }
 
 template <int D>
@@ -1223,16 +1280,26 @@ size_t decode_smem(int M, int heads) {
   return (size_t)decode_smem_bytes<D>(M, heads);
 }
 
+template <int D, int kKind, bool kLanes>
+cudaError_t launch_split_layout(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                const SplitParams& a, dim3 grid, cudaStream_t stream, const char* what,
+                                const char** failed) {
+  const size_t smem = split_smem<D, kKind>();
+  *failed = "cudaFuncSetAttribute(split_kernel)";
+  cudaError_t e =
+      cudaFuncSetAttribute(split_kernel<D, kKind, kLanes>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  split_kernel<D, kKind, kLanes><<<grid, kThreads, smem, stream>>>(mq, mk, mv, a);
+  *failed = what;
+  return cudaGetLastError();
+}
+
+// M <= 64 takes the lanes layout (two token tiles per step)
 template <int D, int kKind>
 cudaError_t launch_split(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const SplitParams& a,
                          dim3 grid, cudaStream_t stream, const char* what, const char** failed) {
-  const size_t smem = split_smem<D, kKind>();
-  *failed = "cudaFuncSetAttribute(split_kernel)";
-  cudaError_t e = cudaFuncSetAttribute(split_kernel<D, kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  split_kernel<D, kKind><<<grid, kThreads, smem, stream>>>(mq, mk, mv, a);
-  *failed = what;
-  return cudaGetLastError();
+  return a.M <= 64 ? launch_split_layout<D, kKind, true>(mq, mk, mv, a, grid, stream, what, failed)
+                   : launch_split_layout<D, kKind, false>(mq, mk, mv, a, grid, stream, what, failed);
 }
 
 // The passes of one call. The synthesis pass depends on the variant: shared
@@ -1358,11 +1425,13 @@ TcPlan tc_plan(int B, int H, int N, int M, int D, int sms, int forced_splits) {
   TcPlan pl{};
   const long long BH = (long long)B * H;
   const int n_tiles = (N + tc::kTile - 1) / tc::kTile;
+  // one CTA per block of 128 latent rows (M <= 64: one block, its rows
+  // repeated in TMEM lanes 64-127)
   pl.tiles = M <= 64 ? 1 : (M + tc::kTile - 1) / tc::kTile;
-  pl.qgroups = M <= 128 ? 1 : (pl.tiles + 1) / 2;
+  pl.qgroups = pl.tiles;
   pl.streams = 1;  // the token streams of a CTA are merged before its partial is written
-  // token tiles per split: at least 4 (two per slot) when the sequence allows
-  const int splits = tc::choose_splits(BH * pl.qgroups, n_tiles, std::max(1, sms), 4, 8, forced_splits);
+  // token tiles per split: at least 4 when the sequence allows
+  const int splits = tc::choose_splits(BH * pl.qgroups, n_tiles, std::max(1, sms), 4, 12, forced_splits);
   const int tiles_per_split = (n_tiles + splits - 1) / splits;
   pl.split_len = tiles_per_split * tc::kTile;
   pl.splits = (N + pl.split_len - 1) / pl.split_len;

@@ -6,7 +6,7 @@ its cycles, from the clock64 stamps that a trace build records.
 Builds the library with FLAREPP_TRACE, runs a few forward calls of the
 workload, then one traced call per pass (synthesis, encode, decode), and
 prints for each pass: the pipeline fill (kernel start to the first scores),
-the median softmax step and the wait for the next scores of the same slot,
+the median softmax step and the wait for the next scores of the same stream,
 the issuing threads' median time to issue the products and the next
 scores, and the drain and epilogue after the last step.
 """
@@ -42,25 +42,23 @@ def report(name, st, mhz):
             print(f"  N0 rows {32 * p}-{32 * p + 31}: {len(nz)} tiles, first +{nz[0] - t0}, "
                   f"median gap {np.median(np.diff(nz)):.0f}")
     last = 0
-    for hf in range(2):
-        row = st[SOFTMAX + hf]
+    for g in range(2):
+        row = st[SOFTMAX + g]
         steps, waits, first = [], [], None
-        for k in range(2):
-            j = 0
-            while 4 * j + 2 * k + 1 < LEN and row[4 * j + 2 * k]:
-                s, f = int(row[4 * j + 2 * k]), int(row[4 * j + 2 * k + 1])
-                first = s if first is None else min(first, s)
-                if f:
-                    steps.append(f - s)
-                    last = max(last, f)
-                nxt = 4 * (j + 1) + 2 * k
-                if f and nxt < LEN and row[nxt]:
-                    waits.append(int(row[nxt]) - f)
-                j += 1
+        j = 0
+        while 2 * j + 1 < LEN and row[2 * j]:
+            s, f = int(row[2 * j]), int(row[2 * j + 1])
+            first = s if first is None else min(first, s)
+            if f:
+                steps.append(f - s)
+                last = max(last, f)
+            if f and 2 * (j + 1) < LEN and row[2 * (j + 1)]:
+                waits.append(int(row[2 * (j + 1)]) - f)
+            j += 1
         if first is not None:
-            print(f"  softmax half {hf}: {len(steps)} steps, first scores +{first - t0}, median step "
-                  f"{_med(steps):.0f}, median wait for the slot's next scores {_med(waits):.0f}")
-    for q in range(4):
+            print(f"  softmax stream {g}: {len(steps)} steps, first scores +{first - t0}, median step "
+                  f"{_med(steps):.0f}, median wait for the next scores {_med(waits):.0f}")
+    for q in range(2):
         row = st[ISSUE + q]
         pv, sc, wp = [], [], []
         j = 0
@@ -74,7 +72,7 @@ def report(name, st, mhz):
                 wp.append(int(row[3 * (j + 1)]) - c)
             j += 1
         if j:
-            print(f"  issuer slot {q >> 1} half {q & 1}: {j} steps, median cycles: products {_med(pv):.0f}, "
+            print(f"  issuer of stream {q}: {j} steps, median cycles: products {_med(pv):.0f}, "
                   f"next scores {_med(sc):.0f}, wait for P {_med(wp):.0f}")
     epi = [int(v) - t0 if v else None for v in st[EPI, :3]]
     print(f"  last softmax step done +{last - t0 if last else -1}; epilogue (drain, partials written, "
