@@ -238,10 +238,13 @@ def measured_traffic(workload: str, kernel: str, src: str = TC_SOURCE, prof: str
     return None
 
 
-def workload_string(name: str, variant: str = "flarepp") -> str:
-    """The ``config.workload`` string, the same for both arms of the bench."""
+def workload_string(name: str, variant: str = "flarepp", tokens: int = 0) -> str:
+    """The ``config.workload`` string, the same for both arms of the bench
+    (``tokens`` > 0: the workload cut to that many tokens per head, a
+    profiling case, named as such)."""
     s, dtype = workloads.CONFIGS[name][0], workloads.CONFIGS[name][1]
-    return (f"{name}: B={s.B} H={s.H} N={s.N} M={s.M} D={s.D} {dtype}"
+    n = tokens if tokens > 0 else s.N
+    return (f"{name}{' cut to N=' + str(n) if tokens > 0 else ''}: B={s.B} H={s.H} N={n} M={s.M} D={s.D} {dtype}"
             + ("" if variant == "flarepp" else f", {variant} mixer"))
 
 
@@ -252,7 +255,7 @@ def run_ours(args, rank, world, local_rank):
 
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    wl = workloads.config(args.workload)
+    wl = workloads.config(args.workload, **({"N": args.tokens} if args.tokens > 0 else {}))
     s = wl.shape
     dev, host = upload(wl, torch, device, args.variant)
     tdtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
@@ -354,7 +357,7 @@ def run_ours(args, rank, world, local_rank):
         "ms_median": round(float(np.median(ms)), 5), "ms_min": round(float(min(ms)), 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic (seeded, shapes of the paper's workloads)",
-        "config": {"workload": workload_string(args.workload, args.variant),
+        "config": {"workload": workload_string(args.workload, args.variant, args.tokens),
                    "global_batch": s.B * world, "seq_len": s.N, "latents": s.M, "head_dim": s.D,
                    "heads": s.H, "parallelism": f"replicas x{world}" if world > 1 else "single",
                    "l2": "512 MB flush before every timed step"},
@@ -369,8 +372,8 @@ def run_ours(args, rank, world, local_rank):
         "impl": "ours",
     }
     rl = line["roofline"]
-    rl["traffic"] = (measured_traffic(args.workload, rl["kernel"]) if args.variant == "flarepp"
-                     else None)
+    rl["traffic"] = (measured_traffic(args.workload, rl["kernel"])
+                     if args.variant == "flarepp" and args.tokens <= 0 else None)
     return line
 
 
@@ -693,6 +696,8 @@ def main():
     ap.add_argument("--variant", default="flarepp", choices=sorted(VARIANT_INPUTS),
                     help="mixer: FLARE++ (default), separate synthesis values, simplified "
                          "FLARE++, or FLARE")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling only: cut the workload to this many tokens per head (mixer op)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
