@@ -931,6 +931,20 @@ struct DecodeParams {
   int fail_wait;       // test only: P barrier of stream 0, buffer 0 expects one arrival too many
 };
 
+// The decode's TMEM per stream, two layouts. Few route blocks per tile
+// (M <= 128, kDbl): two 64-column score buffers (scores issued two steps
+// ahead) and two accumulators that the stream's tiles use in turn, so that a
+// tile's output goes out during the next tile without waiting for its last
+// products. Otherwise: three score buffers (scores three steps ahead) and one
+// accumulator; the output goes out at the next tile's first step.
+template <bool kDbl>
+struct DecLayout {
+  static constexpr int kBufs = kDbl ? 2 : 3;
+  static constexpr uint32_t kColO = kBufs * 64;
+};
+static_assert(DecLayout<true>::kColO + 2 * Layout<32>::kNo <= kGroupCols, "decode accumulators exceed a stream's columns");
+static_assert(DecLayout<false>::kColO + Layout<32>::kNo <= kGroupCols, "decode accumulator exceeds a stream's columns");
+
 // Token-tile ring depth of the decode kernel: a compile-time constant, so
 // that the ring index and phase of a tile cost no division on the issuing
 // threads. With Q and Z of M <= 512 routes resident it still fits.
@@ -944,11 +958,13 @@ __host__ __device__ constexpr int decode_smem_bytes(int M, int heads) {
 }
 static_assert(decode_smem_bytes<32>(512, 1) <= kDecodeSmemLimit, "decode ring does not fit next to Q and Z");
 
-template <int D>
+template <int D, bool kDbl>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_z, const DecodeParams p) {
   using L = Layout<D>;
+  constexpr int kDecBufs = DecLayout<kDbl>::kBufs;
+  constexpr uint32_t kDecColO = DecLayout<kDbl>::kColO;
   extern __shared__ unsigned char smem_raw[];
   __shared__ Shared sh;
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1011,7 +1027,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sh.q_full, 1);
     for (int g = 0; g < 2; ++g) {
-      for (int b = 0; b < kBufs; ++b) {
+      for (int b = 0; b < kDecBufs; ++b) {
         mbar_init(&sh.s_full[g][b], 1);
         mbar_init(&sh.p_full[g][b], 4 + (p.fail_wait && g == 0 && b == 0 ? 1 : 0));
       }
@@ -1073,7 +1089,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // buffers, every ring stage, route block and descriptor moved by adds.
     const int g = warp - kWarpIssue;
     const uint32_t gbase = tmem + g * kGroupCols;
-    const uint32_t dO = gbase + kColO;
     const uint32_t aOnes = smem_u32(sOnes);
     const uint32_t idO = idesc_bf16(128, L::kNo, false, true);
     const uint32_t idS64 = idesc_bf16(128, 64, false, false);
@@ -1103,6 +1118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t par_s = 0u;
     uint64_t ks = dK0 + static_cast<uint64_t>(g) * kKStep, qs = q_head(head_slot(g) * head_bytes);
     int tp = g, bp = 0, stage_p = g;
+    uint32_t dO = gbase + kDecColO;  // the accumulator of the products' tile (by the stream's tile parity)
     uint64_t zp = z_head(head_slot(g) * head_bytes);
     // scores of the next step into buffer b (past the end: the ones tile
     // against itself, a proof-only set)
@@ -1153,6 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_elect(&sh.o_full[g]);
         bp = 0;
         tp += 2;
+        if (kDbl) dO = dO == gbase + kDecColO ? gbase + kDecColO + L::kNo : gbase + kDecColO;
         stage_p += 2;
         if (stage_p >= stages) stage_p -= stages;
         zp = z_head(head_slot(tp) * head_bytes);
@@ -1161,27 +1178,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     bool ok = U > 0 && warp_wait(sh, &sh.q_full, 0);
-    // the first three score sets
+    // the first two score sets
 #pragma unroll
-    for (int b = 0; b < kBufs; ++b) {
+    for (int b = 0; b < kDecBufs; ++b) {
       if (!ok) break;
       ok = issue_s(b < U, b);
     }
+    // step j with buffer b: the products, then the scores of step j + kDecBufs
+    // into the same buffer (U + kDecBufs - 2 is the last one issued: proof-only
+    // sets past the end)
     auto step = [&](int j, int b, uint32_t par) -> bool {
       if (!warp_wait(sh, &sh.p_full[g][b], par)) return false;
       FLAREPP_TR(tr_on && lane == 0, kTrIssue + g, 3 * j);
       tc_fence_after();
       issue_pv(b);
       FLAREPP_TR(tr_on && lane == 0, kTrIssue + g, 3 * j + 1);
-      if (j + kBufs <= U + 1 && !issue_s(j + kBufs < U, b)) return false;
+      if (j + kDecBufs <= U + kDecBufs - 2 && !issue_s(j + kDecBufs < U, b)) return false;
       FLAREPP_TR(tr_on && lane == 0, kTrIssue + g, 3 * j + 2);
       return true;
     };
     uint32_t par = 0u;
-    for (int j = 0; ok && j < U; j += kBufs, par ^= 1u) {
+    for (int j = 0; ok && j < U; j += kDecBufs, par ^= 1u) {
       ok = step(j, 0, par);
       if (ok && j + 1 < U) ok = step(j + 1, 1, par);
-      if (ok && j + 2 < U) ok = step(j + 2, 2, par);
+      if (kDecBufs == 3 && ok && j + 2 < U) ok = step(j + 2, 2, par);
     }
     mma_commit_elect(&sh.drain);
     mbar_wait(&sh.drain, 0, sh.wait_limit);
@@ -1191,9 +1211,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t gbase = tmem + lane_base + g * kGroupCols;
-    const uint32_t tO = gbase + kColO;
     const float c = rsqrtf((float)D) * kLog2e;
-    const int U = stream_steps(g);
+    // the accumulator of the stream's i-th tile (two, by tile parity, in the
+    // double layout)
+    auto acc_of = [&](int i) { return gbase + kDecColO + (kDbl ? (i & 1) * L::kNo : 0u); };
 #ifdef FLAREPP_TRACE
     const bool tr_sm = tr_on && lane == 0 && (warp == kWarpSoftmax || warp == kWarpSoftmax + 4);
 #endif
@@ -1204,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (!done) return false;
       float z[D];
-      const float l = load_acc<D>(tO, z);
+      const float l = load_acc<D>(acc_of(i), z);
       const int hs = head_slot(t);
       const int tok = (first + t - hs * n_tiles) * kTile + row;
       if (tok < p.N) {
@@ -1221,7 +1242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wlast = p.M - 64 * (nsub - 1);  // routes of a tile's last block (16..64)
     const int ntiles = T > g ? (T - g + 1) / 2 : 0;
     int bf = 0, j = 0, i = 0;
-    uint32_t par = 0u;  // phase parity of step j's barriers: (j / 3) & 1
+    uint32_t par = 0u;  // phase parity of step j's barriers: (j / kDecBufs) & 1
     // Step j: route block b of the stream's i-th tile. kRagged: the last
     // block of a tile when M is not a multiple of 64 (its columns at or past
     // `wlast` count as absent); every other block has no test of its columns.
@@ -1235,15 +1256,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // from its own first route block and its accumulator starts empty
       if (b == 0) acc = false;
       const bool moved = softmax_step<kRagged>(tS, kRagged ? wlast : 64, b == 0, c, r, r_old);
-      // the previous tile's output goes out before this step's products
-      // overwrite the accumulator
-      if (b == 0 && i > 0 && !emit(i - 1, g + 2 * (i - 1))) return false;
-      const int bp = bf == 0 ? 2 : (bf == 1 ? 0 : 1);  // buffer of step j + 2 and its phase
-      const bool ok2 = finish_step<D>(sh, &sh.p_full[g][bf], tO, r, r_old, acc, moved, &sh.s_full[g][bp],
-                                      bf == 0 ? par : par ^ 1u);
+      // The previous tile's output goes out before the products that
+      // overwrite its accumulator: in the double layout at this tile's last
+      // step (its own last products were issued a whole tile ago), otherwise
+      // at this tile's first step.
+      if (b == (kDbl ? nsub - 1 : 0) && i > 0 && !emit(i - 1, g + 2 * (i - 1))) return false;
+      // proof of the previous products: the scores issued after them, those
+      // of step j + kDecBufs - 1
+      const int bp = kDbl ? (bf ^ 1) : (bf == 0 ? 2 : (bf == 1 ? 0 : 1));
+      const bool ok2 = finish_step<D>(sh, &sh.p_full[g][bf], acc_of(i), r, r_old, acc, moved,
+                                      &sh.s_full[g][bp], bf == 0 ? par : par ^ 1u);
       FLAREPP_TR(tr_sm, kTrSoftmax + g, 2 * j + 1);
       acc = true;
-      if (bf == kBufs - 1) {
+      if (bf == kDecBufs - 1) {
         bf = 0;
         par ^= 1u;
       } else {
@@ -1385,10 +1410,11 @@ cudaError_t forward_d(const DeviceProblem& pr, const TcPlan& pl, const TcWorkspa
     d.fail_wait = pr.fail_wait == 3;
     const size_t smem = decode_smem<D>(pr.M, pl.decode_heads);
     *failed = "cudaFuncSetAttribute(decode)";
-    if ((e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-        cudaSuccess)
+    // two route blocks or fewer per tile: the double-accumulator layout
+    auto kernel = pr.M <= 128 ? decode_kernel<D, true> : decode_kernel<D, false>;
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
-    decode_kernel<D><<<pl.decode_ctas, kThreads, smem, stream>>>(m_k, m_qdec, m_zdec, d);
+    kernel<<<pl.decode_ctas, kThreads, smem, stream>>>(m_k, m_qdec, m_zdec, d);
     *failed = "launch decode";
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
