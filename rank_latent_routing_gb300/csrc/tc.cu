@@ -951,7 +951,7 @@ static_assert(DecLayout<false>::kColO + Layout<32>::kNo <= kGroupCols, "decode a
 // Token-tile ring depth of the decode kernel: a compile-time constant, so
 // that the ring index and phase of a tile cost no division on the issuing
 // threads. With Q and Z of M <= 512 routes resident it still fits.
-constexpr int kDecodeStages = kMaxStages;
+constexpr int kDecodeStages = 12;
 // At most this many heads' Q and Z per CTA, within this much shared memory.
 constexpr int kDecodeHeads = 4;
 constexpr int kDecodeSmemLimit = 220 * 1024;
